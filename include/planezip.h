@@ -1,0 +1,112 @@
+/*
+ * planezip.h — C ABI of the PlaneZip block codec on GB300 (sm_103a).
+ *
+ * The codec is the one of "PlaneZip: Lossless Bit-Plane Compression of
+ * Training Activations Offloaded over PCIe" (arXiv:2610.25033v1),
+ * Section III-A "Codec" and "Stream format": a tensor is cut into 128-byte
+ * blocks, each block is coded as the smallest of ZVC, DBX, BX, ZBX and the
+ * raw block behind a 3-bit tag, and 32 blocks form a 4 KB chunk that is
+ * byte-aligned, carries a 16-bit size, and is stored raw if coding would
+ * grow it.
+ *
+ * Stream layout produced and consumed here (for nbytes of input, C chunks):
+ *   bytes [0, 2C)            C little-endian uint16 chunk sizes L_c
+ *   bytes [2C, 2C + sum L)   chunk payloads, concatenated, byte-aligned
+ * A chunk with L_c equal to its raw size (4096, or the tail size for the
+ * last chunk) is stored verbatim. The bit-level format (field orders, code
+ * patterns, tie-breaks) is written out in
+ * lossless_bit_plane_gb300/csrc/pz_format.cuh.
+ *
+ * Conventions for every call:
+ *   - "d_" pointers are DEVICE pointers of the current CUDA device; the
+ *     caller owns every buffer. The calls allocate nothing.
+ *   - Work is enqueued on `stream` and the call returns without waiting;
+ *     device-side results are valid after the stream is synchronized.
+ *   - A non-PZ_OK return means nothing was enqueued (argument errors) or a
+ *     launch failed (PZ_ERR_CUDA, with the CUDA error left to the caller's
+ *     next cudaGetLastError()).
+ *   - Thread-safe and stateless apart from per-device caches of device
+ *     attributes and of the driver's tensor-map encoder.
+ */
+#ifndef PLANEZIP_H
+#define PLANEZIP_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pz_stream_t; /* == cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  PZ_OK = 0,
+  PZ_ERR_ARG = 1,      /* null pointer, bad width, misaligned pointer, stream too short */
+  PZ_ERR_CAPACITY = 2, /* out_capacity below pz_max_compressed_bytes(nbytes) */
+  PZ_ERR_CORRUPT = 3,  /* (device status) malformed compressed stream */
+  PZ_ERR_CUDA = 4,     /* a CUDA launch or memset failed */
+  PZ_ERR_TIMEOUT = 5   /* (device status) an inter-chunk wait hit its iteration limit */
+} pz_status;
+
+/* Bytes the caller must allocate for pz_compress's output buffer when
+ * compressing nbytes: the largest stream, 2*C + nbytes (every chunk raw),
+ * rounded up to 16, plus the encoder's scratch area (8 bytes per chunk + 64)
+ * that lives in the tail of the same buffer. Host-only, pure function.
+ * Source: Section III-A "Stream format" (16-bit size per chunk; a chunk that
+ * would grow is stored raw, so the stream never exceeds 2*C + nbytes). */
+size_t pz_max_compressed_bytes(size_t nbytes);
+
+/* Compress nbytes at d_in into d_out.
+ * Source: Section III-A "Codec" (block split, symbol width from the element
+ * type, the five candidates, smallest kept with a 3-bit tag) and "Stream
+ * format" (chunks, headers, raw fallback, prefix-sum location).
+ *   d_in          device, >= nbytes readable; 16-byte aligned.
+ *   nbytes        input size in bytes; any value (0 gives an empty stream).
+ *   elem_width    element size in bytes: 2 selects 16-bit symbols (BF16,
+ *                 64 per block); any other positive value selects 32-bit
+ *                 symbols (FP32 and all other types, 32 per block).
+ *   d_out         device, out_capacity bytes; 16-byte aligned. Receives the
+ *                 stream in [0, *d_total_bytes); bytes past the stream are
+ *                 scratch and are left unspecified.
+ *   out_capacity  must be >= pz_max_compressed_bytes(nbytes).
+ *   d_total_bytes device uint64: set to the stream length 2*C + sum(L)
+ *                 (the compressed size the paper's engine reports, Section
+ *                 III-B), or to UINT64_MAX if a device-side wait timed out.
+ *   stream        CUDA stream.
+ * Errors: PZ_ERR_ARG (null/misaligned pointer, elem_width <= 0),
+ * PZ_ERR_CAPACITY, PZ_ERR_CUDA. Calls that overlap on the GPU must use
+ * distinct d_out buffers. */
+pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width,
+                      void *d_out, size_t out_capacity,
+                      unsigned long long *d_total_bytes, pz_stream_t stream);
+
+/* Decompress a stream produced by pz_compress (or the identical CPU
+ * oracle) back into nbytes at d_out.
+ * Source: Section III-A "Stream format" (chunks located by a prefix sum
+ * over the headers and decoded in parallel) and the inverse of each
+ * candidate of Section III-A "Codec".
+ *   d_in        device, comp_bytes readable; 16-byte aligned.
+ *   comp_bytes  bytes available at d_in: >= 2*C, and the stream's own
+ *               length 2*C + sum(L) must not exceed it (trailing bytes are
+ *               ignored).
+ *   elem_width  the width given to pz_compress.
+ *   d_out       device, nbytes writable; 16-byte aligned. Only [0, nbytes)
+ *               is written.
+ *   nbytes      the original size.
+ *   d_status    device int: set to PZ_OK, or PZ_ERR_CORRUPT if any field of
+ *               the stream is malformed (bad size, tag, code, position,
+ *               overrun, non-zero padding). The output is then unspecified
+ *               but no byte outside [0, nbytes) is written, and reads stay
+ *               inside the 16-byte-aligned granules that [0, comp_bytes)
+ *               touches.
+ * Errors: PZ_ERR_ARG (null/misaligned pointer, elem_width <= 0,
+ * comp_bytes < 2*C), PZ_ERR_CUDA. */
+pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width,
+                        void *d_out, size_t nbytes, int *d_status,
+                        pz_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLANEZIP_H */

@@ -1,0 +1,113 @@
+"""ctypes binding of ``libplanezip.so`` — argument marshalling only.
+
+The functions mirror the C ABI in ``include/planezip.h`` one to one
+(``pz_max_compressed_bytes``, ``pz_compress``, ``pz_decompress``); every step
+of the codec runs in the library's CUDA kernels. The ``*_tensor`` helpers
+below use PyTorch only to allocate device memory and to name the current
+stream. There is no fallback: if the library is missing or cannot be loaded,
+these calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+LIB_PATH = Path(__file__).resolve().parent / "libplanezip.so"
+
+PZ_OK, PZ_ERR_ARG, PZ_ERR_CAPACITY, PZ_ERR_CORRUPT, PZ_ERR_CUDA, PZ_ERR_TIMEOUT = range(6)
+STATUS_NAMES = {0: "PZ_OK", 1: "PZ_ERR_ARG", 2: "PZ_ERR_CAPACITY", 3: "PZ_ERR_CORRUPT",
+                4: "PZ_ERR_CUDA", 5: "PZ_ERR_TIMEOUT"}
+EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress")
+
+_lib = None
+
+
+class PlaneZipError(RuntimeError):
+    def __init__(self, where: str, status: int):
+        super().__init__(f"{where} returned {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load libplanezip.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with lossless_bit_plane_gb300.build.build()")
+        L = ctypes.CDLL(str(LIB_PATH))
+        sz, vp = ctypes.c_size_t, ctypes.c_void_p
+        L.pz_max_compressed_bytes.argtypes = [sz]
+        L.pz_max_compressed_bytes.restype = sz
+        L.pz_compress.argtypes = [vp, sz, ctypes.c_int, vp, sz, vp, vp]
+        L.pz_compress.restype = ctypes.c_int
+        L.pz_decompress.argtypes = [vp, sz, ctypes.c_int, vp, sz, vp, vp]
+        L.pz_decompress.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def pz_max_compressed_bytes(nbytes: int) -> int:
+    return int(load().pz_max_compressed_bytes(nbytes))
+
+
+def pz_compress(d_in: int, nbytes: int, elem_width: int, d_out: int, out_capacity: int,
+                d_total_bytes: int, stream: int = 0) -> int:
+    """Raw C-ABI call with integer device addresses; returns the status code."""
+    return int(load().pz_compress(d_in or None, nbytes, elem_width, d_out or None, out_capacity,
+                                  d_total_bytes or None, stream or None))
+
+
+def pz_decompress(d_in: int, comp_bytes: int, elem_width: int, d_out: int, nbytes: int,
+                  d_status: int, stream: int = 0) -> int:
+    return int(load().pz_decompress(d_in or None, comp_bytes, elem_width, d_out or None, nbytes,
+                                    d_status or None, stream or None))
+
+
+# ---------------------------------------------------------------- torch glue
+
+def _current_stream_handle(device) -> int:
+    import torch
+
+    return int(torch.cuda.current_stream(device).cuda_stream)
+
+
+def compress_tensor(x, elem_width: int, out=None, total=None):
+    """Compress the bytes of a contiguous CUDA tensor.
+
+    Returns ``(out, total)``: ``out`` is a uint8 CUDA tensor of
+    ``pz_max_compressed_bytes`` bytes whose first ``total.item()`` bytes are
+    the stream; ``total`` is a 1-element int64 CUDA tensor. Asynchronous on
+    the current stream."""
+    import torch
+
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("compress_tensor needs a contiguous CUDA tensor")
+    nbytes = x.numel() * x.element_size()
+    cap = pz_max_compressed_bytes(nbytes)
+    if out is None:
+        out = torch.empty(max(cap, 16), dtype=torch.uint8, device=x.device)
+    if total is None:
+        total = torch.empty(1, dtype=torch.int64, device=x.device)
+    rc = pz_compress(x.data_ptr(), nbytes, elem_width, out.data_ptr(), out.numel(), total.data_ptr(),
+                     _current_stream_handle(x.device))
+    if rc != PZ_OK:
+        raise PlaneZipError("pz_compress", rc)
+    return out, total
+
+
+def decompress_tensor(stream_buf, comp_bytes: int, elem_width: int, nbytes: int, out=None, status=None):
+    """Decompress ``comp_bytes`` of a uint8 CUDA tensor into ``nbytes``.
+
+    Returns ``(out, status)``; ``status`` is a 1-element int32 CUDA tensor
+    holding PZ_OK or PZ_ERR_CORRUPT once the stream completes."""
+    import torch
+
+    if out is None:
+        out = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=stream_buf.device)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=stream_buf.device)
+    rc = pz_decompress(stream_buf.data_ptr(), comp_bytes, elem_width, out.data_ptr(), nbytes,
+                       status.data_ptr(), _current_stream_handle(stream_buf.device))
+    if rc != PZ_OK:
+        raise PlaneZipError("pz_decompress", rc)
+    return out, status

@@ -1,0 +1,162 @@
+// api.cu — the C ABI of include/planezip.h: argument checks, the encoder's
+// scratch layout in the output buffer's tail, the TMA tensor map of the
+// input, launch shapes, and the launches. No device memory is allocated.
+//
+// Paper: "PlaneZip: Lossless Bit-Plane Compression of Training Activations
+// Offloaded over PCIe" (arXiv:2610.25033v1), Section III-A "Codec" and
+// "Stream format" (what the two launched kernels compute).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/planezip.h"
+#include "pz_kernels.h"
+
+namespace {
+
+constexpr size_t kChunk = 4096;
+constexpr int kMaxDevices = 64;
+
+size_t num_chunks(size_t nbytes) { return (nbytes + kChunk - 1) / kChunk; }
+size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int enc_ctas_per_sm[2] = {0, 0};
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+// Per-device launch facts, computed once with the device current.
+cudaError_t device_info(DeviceInfo &out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const size_t smem = pz::encode_smem_bytes();
+    for (int w = 0; w < 2; ++w) {
+      const void *k = pz::encode_kernel_ptr(w == 1);
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.enc_ctas_per_sm[w], k, pz::encode_threads(),
+                                                             smem)) != cudaSuccess)
+        return e;
+      if (d.enc_ctas_per_sm[w] < 1) return cudaErrorInvalidConfiguration;
+    }
+    if (!g_encode_tiled) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+      g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  out = d;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pz_max_compressed_bytes(size_t nbytes) {
+  const size_t C = num_chunks(nbytes);
+  return align16(2 * C + nbytes) + 8 * C + 64;
+}
+
+pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width, void *d_out, size_t out_capacity,
+                      unsigned long long *d_total_bytes, pz_stream_t stream) {
+  if (elem_width <= 0 || !d_total_bytes) return PZ_ERR_ARG;
+  const size_t C = num_chunks(nbytes);
+  if (nbytes && (!d_in || !d_out)) return PZ_ERR_ARG;
+  if (nbytes && (!aligned16(d_in) || !aligned16(d_out))) return PZ_ERR_ARG;
+  if (C > 0x7FFFFFFFu || nbytes / 128 > 0xFFFFFFFFull) return PZ_ERR_ARG;
+  if (out_capacity < pz_max_compressed_bytes(nbytes)) return PZ_ERR_CAPACITY;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
+  if (nbytes == 0) return PZ_OK;
+
+  DeviceInfo info;
+  if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
+
+  uint8_t *out = static_cast<uint8_t *>(d_out);
+  uint8_t *scratch = out + align16(2 * C + nbytes);
+  if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
+
+  pz::EncodeArgs a;
+  a.in = static_cast<const uint8_t *>(d_in);
+  a.out = out;
+  a.status = reinterpret_cast<unsigned long long *>(scratch);
+  a.ticket = reinterpret_cast<unsigned int *>(scratch + 8 * C);
+  a.total = d_total_bytes;
+  a.nbytes = nbytes;
+  a.num_chunks = (uint32_t)C;
+  a.tma_rows = nbytes / 128;
+
+  alignas(64) CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  if (a.tma_rows > 0) {
+    cuuint64_t dims[2] = {32, (cuuint64_t)a.tma_rows};  // 32 x u32 per 128-byte row
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(d_in), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return PZ_ERR_CUDA;
+  }
+
+  const bool w16 = (elem_width == 2);
+  const int warps = pz::encode_warps();
+  size_t grid = (size_t)info.enc_ctas_per_sm[w16 ? 1 : 0] * info.sms;
+  const size_t need = (C + warps - 1) / warps;
+  if (grid > need) grid = need;
+  void *args[2] = {&tmap, &a};
+  if (cudaLaunchKernel(pz::encode_kernel_ptr(w16), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
+                       pz::encode_smem_bytes(), s) != cudaSuccess)
+    return PZ_ERR_CUDA;
+  return PZ_OK;
+}
+
+pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, void *d_out, size_t nbytes,
+                        int *d_status, pz_stream_t stream) {
+  if (elem_width <= 0 || !d_status) return PZ_ERR_ARG;
+  const size_t C = num_chunks(nbytes);
+  if (nbytes && (!d_in || !d_out)) return PZ_ERR_ARG;
+  if (nbytes && (!aligned16(d_in) || !aligned16(d_out))) return PZ_ERR_ARG;
+  if (C > 0x7FFFFFFFu) return PZ_ERR_ARG;
+  if (comp_bytes < 2 * C) return PZ_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_status, 0, sizeof(int), s) != cudaSuccess) return PZ_ERR_CUDA;
+  if (C == 0) return PZ_OK;
+
+  pz::DecodeArgs a;
+  a.in = static_cast<const uint8_t *>(d_in);
+  a.comp_bytes = comp_bytes;
+  a.out = static_cast<uint8_t *>(d_out);
+  a.nbytes = nbytes;
+  a.status = d_status;
+  a.num_chunks = (uint32_t)C;
+  const size_t per = (size_t)pz::decode_chunks_per_cta();
+  const size_t grid = (C + per - 1) / per;
+  void *args[1] = {&a};
+  if (cudaLaunchKernel(pz::decode_kernel_ptr(elem_width == 2), dim3((unsigned)grid), dim3(pz::decode_threads()),
+                       args, 0, s) != cudaSuccess)
+    return PZ_ERR_CUDA;
+  return PZ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,739 @@
+// encode.cu — PlaneZip block encoder for sm_103a.
+//
+// Paper: "PlaneZip: Lossless Bit-Plane Compression of Training Activations
+// Offloaded over PCIe" (arXiv:2610.25033v1), Section III-A "Codec" (per
+// 128-byte block: ZVC, DBX, BX, ZBX and raw; the smallest is kept behind a
+// 3-bit tag; BPC's plane prefix code) and "Stream format" (32 blocks per
+// byte-aligned 4 KB chunk with a 16-bit size; a chunk that would grow is
+// stored raw); Section II-B (BPC's Delta-BitPlane-XOR).
+//
+// GPU design (one kernel does load, classify, select, emit, scan, scatter):
+//  - Persistent warps take chunks in ticket order (atomic counter). A warp
+//    owns a 4 KB chunk; LANE b OWNS BLOCK b and works on it alone, so the
+//    per-block work is SIMD over 32 blocks rather than cooperative.
+//  - The chunk arrives by a 2D TMA tile load (32 rows x 128 B, 128-byte
+//    swizzle) into a double-buffered shared stage; the next chunk's load is
+//    in flight while the current one is coded. The swizzle makes each lane's
+//    row read (8 x 16 B) bank-conflict free.
+//  - Candidate sizes come from plane CLASSES, computed bit-sliced over the
+//    32 words a lane holds: the XOR of adjacent planes is the Gray code
+//    g = v ^ (v >> 1) of each symbol, and per-plane "any one", "two or more",
+//    "three or more", "all ones", "adjacent pair" and "pre-XOR plane zero"
+//    flags are plain OR/AND accumulations across words. BF16 runs the same
+//    word loop on two 16-bit symbols per word (symbols j and j+32).
+//  - Only the winning candidate is materialised: its planes come from one
+//    32x32 bit transpose in registers, and its codes go into a shared chunk
+//    buffer through an LSB-first writer at the block's bit offset (a warp
+//    prefix sum over the lanes' block sizes).
+//  - Chunk offsets come from a single-pass decoupled look-back over 8-byte
+//    status words (flag | value) in the scratch tail of the output buffer,
+//    with a bounded spin; the warp then copies its chunk to its final byte
+//    offset with aligned 16-byte stores and byte stores at the two edges.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pz_device.cuh"
+#include "pz_format.cuh"
+#include "pz_kernels.h"
+
+namespace pz {
+
+constexpr uint64_t kFlagAgg = 1ull << 62;
+constexpr uint64_t kFlagInc = 2ull << 62;
+constexpr uint64_t kValueMask = (1ull << 62) - 1;
+constexpr uint32_t kLookbackSpinLimit = 1u << 21;
+constexpr uint32_t kMbarPollLimit = 1u << 24;
+
+// ------------------------------------------------------------ cost helpers
+
+// Zero planes (bits of Z, only the first P bits may be set) form maximal
+// runs: a run of one costs 3 bits, a longer run 2 + K bits.
+__device__ __forceinline__ int run_cost(uint64_t Z, int K) {
+  uint64_t start = Z & ~(Z << 1);
+  uint64_t single = start & ~(Z >> 1);
+  int R = __popcll(start), S = __popcll(single);
+  return 3 * S + (2 + K) * (R - S);
+}
+
+// Cost of the non-zero planes NZ of width W (position field p): planes that
+// are all ones or whose pre-XOR plane is zero (c5) take the 5-bit code, or
+// verbatim if shorter; planes with one or two adjacent ones take 5 + p (or
+// verbatim); the rest are verbatim, 1 + W.
+__device__ __forceinline__ int nonzero_cost(uint64_t NZ, uint64_t A, uint64_t PX, uint64_t ST,
+                                            int W, int p) {
+  uint64_t c5 = (A | PX) & NZ;
+  uint64_t cm = ST & NZ & ~c5;
+  uint64_t cv = NZ & ~(c5 | cm);
+  int lv = 1 + W;
+  int l5 = min(5, lv), lm = min(5 + p, lv);
+  return l5 * __popcll(c5) + lm * __popcll(cm) + lv * __popcll(cv);
+}
+
+// Class of a single plane given as a word: 0 zero, else its code length.
+template <typename T>
+__device__ __forceinline__ int single_plane_len(T X, T full, int W, int p) {
+  if (X == 0) return 0;
+  int ones = (sizeof(T) == 8) ? __popcll((uint64_t)X) : __popc((uint32_t)X);
+  int lv = 1 + W;
+  if (X == full) return min(5, lv);
+  bool adj2 = (ones == 2) && ((X & (X >> 1)) != 0);
+  if (ones == 1 || adj2) return min(5 + p, lv);
+  return lv;
+}
+
+struct Sizes {
+  int s[5];
+};
+
+__device__ __forceinline__ void select_min(const Sizes &z, uint32_t &tag, uint32_t &bits) {
+  tag = 0;
+  int best = z.s[0];
+#pragma unroll
+  for (int t = 1; t < 5; ++t)
+    if (z.s[t] < best) {
+      best = z.s[t];
+      tag = t;
+    }
+  bits = (uint32_t)best;
+}
+
+// ------------------------------------------------------------ FP32 classify
+// s: the block's 32 symbols. Returns the five candidate sizes (tag excluded).
+__device__ __forceinline__ Sizes classify32(const uint32_t (&s)[32]) {
+  uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0;  // BX
+  uint32_t nz = 0, zn = 0, adjz = 0, last = 0;                            // ZBX / ZVC
+  uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Bw = 0, gdprev = 0;  // DBX
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    uint32_t x = s[k];
+    uint32_t g = x ^ (x >> 1);
+    ors |= x;
+    c |= b & g;
+    b |= a & g;
+    a |= g;
+    if (k) adj |= gprev & g;
+    andx &= g;
+    gprev = g;
+    uint32_t m = x ? 0xFFFFFFFFu : 0u;
+    nz |= m & (1u << k);
+    zn |= ~g & m;  // some survivor has a 0 in the plane
+    adjz |= last & g;
+    last = x ? g : last;
+    if (k) {
+      uint64_t d = (uint64_t)x - (uint64_t)s[k - 1];
+      uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);  // hi: borrow mask
+      uint32_t gd = lo ^ __funnelshift_r(lo, hi, 1);
+      ord |= lo;
+      Bw |= hi & (1u << (k - 1));
+      cd |= bd & gd;
+      bd |= ad & gd;
+      ad |= gd;
+      if (k > 1) adjd |= gdprev & gd;
+      andd &= gd;
+      gdprev = gd;
+    }
+  }
+  Sizes z;
+  int n = __popc(nz);
+  z.s[kTagZVC] = 32 + 32 * n;
+  z.s[kTagRAW] = 1024;
+  // BX: 32 planes of width 32, top plane 31
+  {
+    uint64_t NZ = a, PX = (~ors & a) & 0x7FFFFFFFu, ST = (a & ~b) | (b & ~c & adj);
+    z.s[kTagBX] = run_cost((uint32_t)~a, 5) + nonzero_cost(NZ, andx, PX, ST, 32, 5);
+  }
+  // ZBX: mask + 32 planes of width n over the survivors
+  if (n == 0) {
+    z.s[kTagZBX] = 32;
+  } else {
+    uint64_t NZ = a, PX = (~ors & a) & 0x7FFFFFFFu, ST = (a & ~b) | (b & ~c & adjz);
+    uint64_t A = ~zn & a;
+    z.s[kTagZBX] = 32 + run_cost((uint32_t)~a, 5) + nonzero_cost(NZ, A, PX, ST, n, ceil_log2_int(n));
+  }
+  // DBX: base + 33 planes of width 31 (plane 32 = borrow plane, the top)
+  {
+    uint64_t NZ = ad, PX = ~ord & ad, ST = (ad & ~bd) | (bd & ~cd & adjd);
+    uint64_t Z = (uint64_t)(uint32_t)~ad | ((uint64_t)(Bw == 0) << 32);
+    z.s[kTagDBX] = 32 + run_cost(Z, 5) + nonzero_cost(NZ, andd, PX, ST, 31, 5) +
+                   single_plane_len<uint32_t>(Bw, 0x7FFFFFFFu, 31, 5);
+  }
+  return z;
+}
+
+// ------------------------------------------------------------ BF16 classify
+// sp: split-packed block (word j = symbol j | symbol j+32 << 16).
+__device__ __forceinline__ Sizes classify16(const uint32_t (&sp)[32]) {
+  uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0, g0 = 0;
+  uint32_t mlo = 0, mhi = 0, zn = 0, adjz = 0, last = 0, fst = 0, seen = 0;
+  uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Blo = 0, Bhi = 0, gdprev = 0,
+           gd0 = 0;
+  const uint32_t s31lo = sp[31] << 16;  // symbol 31 moved to the high half
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    uint32_t x = sp[j];
+    uint32_t g = x ^ ((x >> 1) & 0x7FFF7FFFu);
+    ors |= x;
+    c |= b & g;
+    b |= a & g;
+    a |= g;
+    if (j) adj |= gprev & g;
+    else g0 = g;
+    andx &= g;
+    gprev = g;
+    uint32_t m = halfmask_nonzero(x);
+    mlo |= (m & 1u) << j;
+    mhi |= (m >> 31) << j;
+    zn |= ~g & m;
+    adjz |= last & g;
+    last = (g & m) | (last & ~m);
+    fst |= g & ~seen;
+    seen |= m;
+    // DBX: lo half d_j = s_j - s_{j-1} (j >= 1), hi half d_{j+32} = s_{j+32} - s_{j+31}
+    uint32_t bo;
+    uint32_t d = sub16x2(x, j ? sp[j - 1] : s31lo, bo);
+    if (j == 0) {
+      d &= 0xFFFF0000u;
+      bo &= 0x80000000u;
+    }
+    uint32_t gd = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
+    ord |= d;
+    cd |= bd & gd;
+    bd |= ad & gd;
+    ad |= gd;
+    andd &= (j == 0) ? (gd | 0x0000FFFFu) : gd;
+    if (j) adjd |= gdprev & gd;
+    else gd0 = gd;
+    gdprev = gd;
+    if (j == 0) {
+      Blo |= bo & 0x80000000u;  // d_32's borrow -> plane position 31
+    } else {
+      Blo |= ((bo >> 15) & 1u) << (j - 1);  // d_j -> position j-1
+      Bhi |= (bo >> 31) << (j - 1);         // d_{j+32} -> position j+31
+    }
+  }
+  // combine the two halves (symbols 0..31 and 32..63) into 16-plane masks
+  auto lo = [](uint32_t v) { return v & 0xFFFFu; };
+  auto hi = [](uint32_t v) { return v >> 16; };
+  Sizes z;
+  int n = __popc(mlo) + __popc(mhi);
+  z.s[kTagZVC] = 64 + 16 * n;
+  z.s[kTagRAW] = 1024;
+  uint32_t a16 = lo(a) | hi(a);
+  uint32_t b16 = lo(b) | hi(b) | (lo(a) & hi(a));
+  uint32_t c16 = lo(c) | hi(c) | (lo(a) & hi(b)) | (lo(b) & hi(a));
+  uint32_t ors16 = lo(ors) | hi(ors);
+  uint32_t Z16 = ~a16 & 0xFFFFu;
+  uint32_t PX16 = (~ors16 & a16) & 0x7FFFu;
+  // BX: 16 planes of width 64; adjacency across the half split is (31, 32)
+  {
+    uint32_t adj16 = lo(adj) | hi(adj) | (lo(gprev) & hi(g0));
+    uint32_t and16 = lo(andx) & hi(andx);
+    uint64_t ST = (a16 & ~b16) | (b16 & ~c16 & adj16);
+    z.s[kTagBX] = run_cost(Z16, 4) + nonzero_cost(a16, and16, PX16, ST, 64, 6);
+  }
+  if (n == 0) {
+    z.s[kTagZBX] = 64;
+  } else {
+    uint32_t adjz16 = lo(adjz) | hi(adjz) | (lo(last) & hi(fst));
+    uint32_t A = ~(lo(zn) | hi(zn)) & a16;
+    uint64_t ST = (a16 & ~b16) | (b16 & ~c16 & adjz16);
+    z.s[kTagZBX] = 64 + run_cost(Z16, 4) + nonzero_cost(a16, A, PX16, ST, n, ceil_log2_int(n));
+  }
+  // DBX: base + 17 planes of width 63 (plane 16 = borrow plane)
+  {
+    uint32_t ad16 = lo(ad) | hi(ad);
+    uint32_t bd16 = lo(bd) | hi(bd) | (lo(ad) & hi(ad));
+    uint32_t cd16 = lo(cd) | hi(cd) | (lo(ad) & hi(bd)) | (lo(bd) & hi(ad));
+    uint32_t adjd16 = lo(adjd) | hi(adjd) | (lo(gdprev) & hi(gd0));
+    uint32_t andd16 = lo(andd) & hi(andd);
+    uint32_t ord16 = lo(ord) | hi(ord);
+    uint64_t Bp = (uint64_t)Blo | ((uint64_t)Bhi << 32);
+    uint64_t ST = (ad16 & ~bd16) | (bd16 & ~cd16 & adjd16);
+    uint64_t Z = (~ad16 & 0xFFFFu) | ((uint64_t)(Bp == 0) << 16);
+    z.s[kTagDBX] = 16 + run_cost(Z, 4) + nonzero_cost(ad16, andd16, ~ord16 & ad16, ST, 63, 6) +
+                   single_plane_len<uint64_t>(Bp, (1ull << 63) - 1, 63, 6);
+  }
+  return z;
+}
+
+// ------------------------------------------------------------------ emit
+
+__device__ __forceinline__ void emit_run(BitWriter &bw, int run, int K) {
+  if (run == 1)
+    bw.put(4u, 3);  // 0 0 1
+  else
+    bw.put(2u | ((uint32_t)(run - 2) << 2), 2 + K);  // 0 1 + (run-2)
+}
+
+template <typename T>
+__device__ __forceinline__ void emit_plane(BitWriter &bw, T X, bool prexor_zero, int W, int p,
+                                           T full) {
+  int ones = (sizeof(T) == 8) ? __popcll((uint64_t)X) : __popc((uint32_t)X);
+  int q = (sizeof(T) == 8) ? (__ffsll((long long)X) - 1) : (__ffs((int)X) - 1);
+  bool A = (X == full);
+  bool T2 = (ones == 2) && ((X >> q) == (T)3);
+  bool S1 = (ones == 1);
+  int best = 1 + W, code = 4;
+  if (S1 && 5 + p <= best) { best = 5 + p; code = 3; }
+  if (T2 && 5 + p <= best) { best = 5 + p; code = 2; }
+  if (prexor_zero && 5 <= best) { best = 5; code = 1; }
+  if (A && 5 <= best) { best = 5; code = 0; }
+  switch (code) {
+    case 0: bw.put(0u, 5); break;                                    // 0 0 0 0 0
+    case 1: bw.put(16u, 5); break;                                   // 0 0 0 0 1
+    case 2: bw.put(8u | ((uint32_t)q << 5), 5 + p); break;           // 0 0 0 1 0 + q
+    case 3: bw.put(24u | ((uint32_t)q << 5), 5 + p); break;          // 0 0 0 1 1 + q
+    default:
+      bw.put(1u, 1);                                                 // 1 + plane
+      bw.put64((uint64_t)X, (uint32_t)W);
+      break;
+  }
+}
+
+// Emit P planes, top first. plane(i) returns X_i (bits >= W are zero).
+template <typename T, typename PlaneFn>
+__device__ __forceinline__ void emit_planes(BitWriter &bw, int top, int W, int p, int K,
+                                            PlaneFn plane) {
+  const T full = (W >= (int)(8 * sizeof(T))) ? ~(T)0 : (((T)1 << W) - 1);
+  int run = 0;
+  T Pup = 0;
+#pragma unroll
+  for (int i = 33; i >= 0; --i) {
+    if (i > top) continue;
+    T X = plane(i);
+    T P = (i == top) ? X : (T)(X ^ Pup);
+    if (X == 0) {
+      ++run;
+    } else {
+      if (run) {
+        emit_run(bw, run, K);
+        run = 0;
+      }
+      emit_plane<T>(bw, X, (i != top) && (P == 0), W, p, full);
+    }
+    Pup = P;
+  }
+  if (run) emit_run(bw, run, K);
+}
+
+// Thread-private compaction scratch: the lane's own 128-byte row of the stage
+// (no other lane reads it once the block is in registers), XOR-swizzled by
+// lane so that lanes at equal indices hit different banks.
+__device__ __forceinline__ uint32_t scratch_addr(uint32_t row, uint32_t word, uint32_t lane) {
+  return row + (((word ^ lane) & 31u) << 2);
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// FP32 emit of the chosen candidate (s is consumed).
+__device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t (&s)[32],
+                                      uint32_t row, uint32_t lane) {
+  if (tag == kTagRAW) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) bw.put(s[k], 32);
+    return;
+  }
+  if (tag == kTagZVC) {
+    uint32_t nz = 0;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) nz |= (s[k] ? 1u : 0u) << k;
+    bw.put(nz, 32);
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (s[k]) bw.put(s[k], 32);
+    return;
+  }
+  if (tag == kTagDBX) {
+    bw.put(s[0], 32);
+    uint32_t Bw = 0;
+#pragma unroll
+    for (int j = 31; j >= 1; --j) {
+      uint64_t d = (uint64_t)s[j] - (uint64_t)s[j - 1];
+      uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);
+      Bw |= hi & (1u << (j - 1));
+      s[j] = lo ^ __funnelshift_r(lo, hi, 1);
+    }
+    s[0] = 0;
+    transpose32(s);
+    emit_planes<uint32_t>(bw, 32, 31, 5, 5,
+                          [&](int i) { return (i == 32) ? Bw : (s[i & 31] >> 1); });
+    return;
+  }
+  int W = 32, p = 5;
+  if (tag == kTagZBX) {
+    uint32_t nz = 0, cnt = 0;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      nz |= (s[k] ? 1u : 0u) << k;
+      if (s[k]) {
+        sts32(scratch_addr(row, cnt, lane), s[k]);
+        ++cnt;
+      }
+    }
+    bw.put(nz, 32);
+    if (cnt == 0) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) s[j] = ((uint32_t)j < cnt) ? lds32(scratch_addr(row, j, lane)) : 0u;
+    W = (int)cnt;
+    p = ceil_log2_int(W);
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) s[j] ^= s[j] >> 1;
+  transpose32(s);
+  emit_planes<uint32_t>(bw, 31, W, p, 5, [&](int i) { return s[i & 31]; });
+}
+
+// BF16 emit of the chosen candidate (sp, split-packed, is consumed).
+__device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t (&sp)[32],
+                                      uint32_t row, uint32_t lane) {
+  if (tag == kTagRAW) {
+#pragma unroll
+    for (int r = 0; r < 32; ++r) bw.put(raw_word_from_split(sp, r), 32);
+    return;
+  }
+  uint32_t mlo = 0, mhi = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    uint32_t m = halfmask_nonzero(sp[j]);
+    mlo |= (m & 1u) << j;
+    mhi |= (m >> 31) << j;
+  }
+  if (tag == kTagZVC) {
+    bw.put(mlo, 32);
+    bw.put(mhi, 32);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (sp[j] & 0xFFFFu) bw.put(sp[j] & 0xFFFFu, 16);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (sp[j] >> 16) bw.put(sp[j] >> 16, 16);
+    return;
+  }
+  if (tag == kTagDBX) {
+    bw.put(sp[0] & 0xFFFFu, 16);
+    const uint32_t s31lo = sp[31] << 16;
+    uint32_t Blo = 0, Bhi = 0;
+#pragma unroll
+    for (int j = 31; j >= 0; --j) {
+      uint32_t bo;
+      uint32_t d = sub16x2(sp[j], j ? sp[j - 1] : s31lo, bo);
+      if (j == 0) {
+        d &= 0xFFFF0000u;
+        bo &= 0x80000000u;
+        Blo |= bo;
+      } else {
+        Blo |= ((bo >> 15) & 1u) << (j - 1);
+        Bhi |= (bo >> 31) << (j - 1);
+      }
+      sp[j] = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
+    }
+    const uint64_t Bp = (uint64_t)Blo | ((uint64_t)Bhi << 32);
+    transpose32(sp);
+    emit_planes<uint64_t>(bw, 16, 63, 6, 4, [&](int i) -> uint64_t {
+      if (i == 16) return Bp;
+      return (uint64_t)(sp[i & 15] >> 1) | ((uint64_t)sp[16 + (i & 15)] << 31);
+    });
+    return;
+  }
+  int W = 64, p = 6;
+  if (tag == kTagZBX) {
+    bw.put(mlo, 32);
+    bw.put(mhi, 32);
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        uint32_t v = half ? (sp[j] >> 16) : (sp[j] & 0xFFFFu);
+        if (v) {
+          sts16(scratch_addr(row, cnt >> 1, lane) + ((cnt & 1u) << 1), v);
+          ++cnt;
+        }
+      }
+    if (cnt == 0) return;
+    uint32_t rw[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) rw[r] = lds32(scratch_addr(row, r, lane));
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      uint32_t keep = (((uint32_t)j < cnt) ? 0x0000FFFFu : 0u) | (((uint32_t)j + 32 < cnt) ? 0xFFFF0000u : 0u);
+      sp[j] = split_word(rw, j) & keep;
+    }
+    W = (int)cnt;
+    p = ceil_log2_int(W);
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) sp[j] ^= (sp[j] >> 1) & 0x7FFF7FFFu;
+  transpose32(sp);
+  emit_planes<uint64_t>(bw, 15, W, p, 4, [&](int i) -> uint64_t {
+    return (uint64_t)sp[i & 15] | ((uint64_t)sp[16 + (i & 15)] << 32);
+  });
+}
+
+// --------------------------------------------------------------- look-back
+
+// Exclusive prefix of the chunk sizes before chunk t. Each chunk publishes
+// (AGG | L) as soon as its size is known and (INC | prefix + L) once its own
+// prefix is known; a warp sums the predecessors' values, 32 at a time,
+// back to the nearest inclusive one.
+__device__ __forceinline__ uint64_t lookback(unsigned long long *status, uint32_t t,
+                                             uint32_t lane, bool &timed_out) {
+  uint64_t excl = 0;
+  int64_t base = (int64_t)t - 1;
+  uint32_t spins = 0;
+  while (base >= 0) {
+    int64_t idx = base - (int64_t)lane;
+    uint64_t v = (idx >= 0) ? ld_relaxed_u64(status + idx) : kFlagInc;
+    uint32_t flag = (uint32_t)(v >> 62);
+    uint32_t pm = __ballot_sync(0xFFFFFFFFu, flag == 2);
+    uint32_t zm = __ballot_sync(0xFFFFFFFFu, flag == 0);
+    uint32_t firstP = pm ? (uint32_t)(__ffs(pm) - 1) : 32u;
+    uint32_t window = (firstP < 31) ? ((2u << firstP) - 1u) : 0xFFFFFFFFu;
+    if (zm & window) {
+      if (++spins > kLookbackSpinLimit) {
+        timed_out = true;
+        break;
+      }
+      __nanosleep(64);
+      continue;
+    }
+    uint64_t val = (lane <= firstP) ? (v & kValueMask) : 0ull;
+    excl += warp_sum_u64(val);
+    if (firstP < 32) break;
+    base -= 32;
+  }
+  return excl;
+}
+
+// ------------------------------------------------------------- copy out
+// Copy L bytes from the shared word buffer to global byte address dst
+// (any alignment): aligned 16-byte stores inside, byte stores at the edges.
+__device__ __forceinline__ void copy_out(const uint32_t *buf, uint32_t L, uint8_t *dst,
+                                         uint32_t lane) {
+  if (L == 0) return;
+  const uint64_t a0 = reinterpret_cast<uint64_t>(dst);
+  const uint64_t v0 = a0 & ~15ull;
+  const uint32_t nvec = (uint32_t)(((a0 + L - 1) & ~15ull) - v0) / 16 + 1;
+  const int nwords = (int)((L + 3) >> 2);
+  for (uint32_t i = lane; i < nvec; i += 32) {
+    const uint64_t A = v0 + 16ull * i;
+    const int o = (int)((int64_t)A - (int64_t)a0);  // source byte of A, may be < 0
+    const int wi = o >> 2;                          // floor
+    const uint32_t sh = (uint32_t)(o & 3) * 8;
+    uint32_t w5[5];
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      int idx = wi + k;
+      w5[k] = (idx >= 0 && idx < nwords) ? buf[idx] : 0u;
+    }
+    uint32_t v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __funnelshift_r(w5[k], w5[k + 1], sh);
+    if (o >= 0 && o + 16 <= (int)L) {
+      *reinterpret_cast<uint4 *>(A) = make_uint4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+      for (int byte = 0; byte < 16; ++byte) {
+        int so = o + byte;
+        if (so >= 0 && so < (int)L)
+          reinterpret_cast<uint8_t *>(A)[byte] = (uint8_t)(v[byte >> 2] >> ((byte & 3) * 8));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+constexpr int kEncWarps = 8;
+constexpr int kOutWords = 1024 + 4;
+
+struct EncSmem {
+  // per warp: stage[2][4096] (1024-aligned), outbuf[kOutWords], mbar[2]
+  static constexpr size_t kStageBytes = 2 * 4096;
+  static constexpr size_t kOutBytes = kOutWords * 4;
+  static constexpr size_t kBytes =
+      1024 + kEncWarps * kStageBytes + kEncWarps * kOutBytes + kEncWarps * 16;
+};
+
+// Byte address of 16-byte unit u of row r in a 128-byte-swizzled stage.
+__device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t u) {
+  return r * 128u + ((u ^ (r & 7u)) << 4);
+}
+
+template <bool W16>
+__global__ void __launch_bounds__(kEncWarps * 32, 2)
+    encode_kernel(const __grid_constant__ CUtensorMap tmap, EncodeArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t lane = lane_id();
+  const uint32_t warp = threadIdx.x >> 5;
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *stage0 = base + warp * EncSmem::kStageBytes;
+  uint32_t *outbuf = reinterpret_cast<uint32_t *>(base + kEncWarps * EncSmem::kStageBytes +
+                                                  warp * EncSmem::kOutBytes);
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(base + kEncWarps * EncSmem::kStageBytes +
+                                                kEncWarps * EncSmem::kOutBytes) +
+                   2 * warp;
+  const uint32_t mb[2] = {smem_u32(mbar), smem_u32(mbar + 1)};
+  if (lane == 0) {
+    mbar_init(mb[0], 1);
+    mbar_init(mb[1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const uint32_t C = p.num_chunks;
+  const uint64_t nbytes = p.nbytes;
+  uint32_t parity[2] = {0, 0};
+  bool failed = false;
+
+  // a chunk is loaded by TMA if its first row lies inside the tensor map
+  auto uses_tma = [&](uint32_t t) { return (uint64_t)t * 32u < p.tma_rows; };
+  auto issue = [&](uint32_t t, int sb) {
+    if (lane == 0 && uses_tma(t)) {
+      mbar_arrive_expect_tx(mb[sb], 4096);
+      tma_load_2d(smem_u32(stage0 + sb * 4096), &tmap, 0, (int)(t * 32u), mb[sb]);
+    }
+  };
+  // plain loads for bytes that the tensor map does not cover
+  auto patch = [&](uint32_t t, uint8_t *st) {
+    const uint64_t c0 = (uint64_t)t * 4096u;
+    const uint32_t raw_len = (uint32_t)umin64(4096u, nbytes - c0);
+    uint32_t from = 0;
+    if (uses_tma(t)) {
+      from = (uint32_t)(umin64((uint64_t)p.tma_rows * 128u, c0 + 4096u) - c0);
+      if (from >= raw_len) return;
+    } else {
+      for (uint32_t u = lane; u < 256; u += 32)
+        *reinterpret_cast<uint4 *>(st + swz(u >> 3, u & 7)) = make_uint4(0, 0, 0, 0);
+      __syncwarp();
+    }
+    for (uint32_t i = from + lane; i < raw_len; i += 32)
+      st[swz(i >> 7, (i >> 4) & 7) + (i & 15)] = p.in[c0 + i];
+    __syncwarp();
+  };
+
+  uint32_t t = 0;
+  if (lane == 0) t = atomicAdd(p.ticket, 1u);
+  t = __shfl_sync(0xFFFFFFFFu, t, 0);
+  int cur = 0;
+  if (t < C) issue(t, cur);
+
+  while (t < C) {
+    uint32_t nt = 0;
+    if (lane == 0) nt = atomicAdd(p.ticket, 1u);
+    nt = __shfl_sync(0xFFFFFFFFu, nt, 0);
+    if (nt < C) issue(nt, cur ^ 1);
+
+    uint8_t *st = stage0 + cur * 4096;
+    if (uses_tma(t)) {
+      if (!mbar_wait(mb[cur], parity[cur], kMbarPollLimit)) failed = true;
+      parity[cur] ^= 1u;
+    }
+    patch(t, st);
+
+    const uint64_t c0 = (uint64_t)t * 4096u;
+    const uint32_t raw_len = (uint32_t)umin64(4096u, nbytes - c0);
+    const uint32_t nblk = (raw_len + 127u) >> 7;
+    const bool active = lane < nblk;
+
+    // the lane's block, 8 x 16 B from its swizzled row
+    uint32_t s[32];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint4 q = *reinterpret_cast<const uint4 *>(st + swz(lane, u));
+      s[4 * u] = q.x;
+      s[4 * u + 1] = q.y;
+      s[4 * u + 2] = q.z;
+      s[4 * u + 3] = q.w;
+    }
+    if (W16) {
+      uint32_t raw[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) raw[k] = s[k];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) s[j] = split_word(raw, j);
+    }
+    Sizes z = W16 ? classify16(s) : classify32(s);
+    uint32_t tag, bits;
+    select_min(z, tag, bits);
+    bits = active ? bits + 3 : 0;
+
+    // block bit offsets: warp prefix sum
+    uint32_t incl = bits;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= (uint32_t)o) incl += v;
+    }
+    const uint32_t total_bits = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const uint32_t off = incl - bits;
+    uint32_t L = (total_bits + 7) >> 3;
+    const bool raw_chunk = L >= raw_len;
+    if (raw_chunk) L = raw_len;
+    if (lane == 0) st_relaxed_u64(p.status + t, (t == 0 ? kFlagInc : kFlagAgg) | L);
+
+    if (!raw_chunk) {
+      const uint32_t nw = (L + 3) / 4 + 1;
+      for (uint32_t i = lane; i < nw; i += 32) outbuf[i] = 0;
+      __syncwarp();
+      if (active) {
+        BitWriter bw;
+        bw.init(outbuf, off, kOutWords);
+        bw.put(tag, 3);
+        const uint32_t row = smem_u32(st + lane * 128u);
+        if (W16)
+          emit16(bw, tag, s, row, lane);
+        else
+          emit32(bw, tag, s, row, lane);
+        bw.flush();
+      }
+    } else {
+      for (uint32_t u = lane; u < 256; u += 32)
+        reinterpret_cast<uint4 *>(outbuf)[u] = *reinterpret_cast<const uint4 *>(st + swz(u >> 3, u & 7));
+    }
+    __syncwarp();
+
+    bool to = false;
+    const uint64_t excl = (t == 0) ? 0 : lookback(p.status, t, lane, to);
+    if (to) failed = true;
+    if (lane == 0) {
+      if (t) st_relaxed_u64(p.status + t, kFlagInc | (excl + L));
+      p.out[2ull * t] = (uint8_t)(L & 0xFF);
+      p.out[2ull * t + 1] = (uint8_t)(L >> 8);
+      if (t == C - 1) atomicMax(p.total, 2ull * C + excl + L);
+    }
+    copy_out(outbuf, L, p.out + 2ull * C + excl, lane);
+
+    __syncwarp();
+    fence_proxy_async_smem();  // generic-proxy use of the stage before the next TMA write
+    t = nt;
+    cur ^= 1;
+  }
+  if (failed && lane == 0) atomicMax(p.total, ~0ull);
+}
+
+template __global__ void encode_kernel<false>(const __grid_constant__ CUtensorMap, EncodeArgs);
+template __global__ void encode_kernel<true>(const __grid_constant__ CUtensorMap, EncodeArgs);
+
+size_t encode_smem_bytes() { return EncSmem::kBytes; }
+int encode_threads() { return kEncWarps * 32; }
+int encode_warps() { return kEncWarps; }
+
+const void *encode_kernel_ptr(bool w16) {
+  return w16 ? reinterpret_cast<const void *>(&encode_kernel<true>)
+             : reinterpret_cast<const void *>(&encode_kernel<false>);
+}
+
+}  // namespace pz

@@ -1,0 +1,40 @@
+// pz_kernels.h — launch-side declarations of the encoder and decoder kernels
+// (argument blocks and launch-shape queries), shared by api.cu and the .cu
+// files that define the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace pz {
+
+struct EncodeArgs {
+  const uint8_t *in;             // input tensor (16-byte aligned)
+  uint8_t *out;                  // stream: headers then payloads
+  unsigned long long *status;    // look-back words, one per chunk, zeroed
+  unsigned int *ticket;          // chunk ticket counter, zeroed
+  unsigned long long *total;     // stream length (atomicMax target), zeroed
+  uint64_t nbytes;
+  uint64_t tma_rows;             // 128-byte rows covered by the tensor map (0: none)
+  uint32_t num_chunks;
+};
+
+struct DecodeArgs {
+  const uint8_t *in;
+  uint64_t comp_bytes;
+  uint8_t *out;
+  uint64_t nbytes;
+  int *status;                   // zeroed; atomicMax of error codes
+  uint32_t num_chunks;
+};
+
+size_t encode_smem_bytes();
+int encode_threads();
+int encode_warps();
+const void *encode_kernel_ptr(bool w16);
+
+int decode_threads();
+int decode_chunks_per_cta();
+const void *decode_kernel_ptr(bool w16);
+
+}  // namespace pz

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA codec, called through the C ABI, against the CPU
+oracle on the same seeded bytes. Streams, chunk sizes and round trips must
+be bit-exact (integer work: no tolerance).
+
+Paper: arXiv:2610.25033v1, Section III-A "Codec" and "Stream format".
+"""
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bit_plane_gb300 import _lib, build
+from lossless_bit_plane_gb300 import workloads as W
+from tests import golden_io
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    _lib.load()
+
+
+from tests.gpu_util import (  # noqa: E402
+    chunk_table,
+    explain_mismatch,
+    gpu_compress,
+    gpu_compress_dev,
+    gpu_decompress,
+    sampled_chunk_parity,
+    to_device,
+)
+
+
+def full_parity(data, ew):
+    data = bytes(data)
+    got = gpu_compress(data, ew)
+    want = oracle.compress(data, ew)
+    assert got == want, explain_mismatch(data, ew, got, want)
+    st, back = gpu_decompress(got, len(data), ew)
+    assert st == _lib.PZ_OK and back == data
+    return got
+
+
+# ------------------------------------------------------------ small cases
+
+@pytest.mark.parametrize("case", golden_io.all_cases(), ids=lambda c: c["name"])
+def test_golden_streams(case):
+    got = gpu_compress(case["input"], case["elem_width"])
+    assert got.hex(" ") == case["stream"].hex(" ")
+    st, back = gpu_decompress(case["stream"], len(case["input"]), case["elem_width"])
+    assert st == 0 and back == case["input"]
+
+
+@pytest.mark.parametrize("ew", [4, 2])
+@pytest.mark.parametrize("which", ["fp32", "bf16"])
+def test_edge_blocks(ew, which):
+    data = W.edge_blocks_fp32() if which == "fp32" else W.edge_blocks_bf16()
+    full_parity(data, ew)
+    # one block per chunk as well (each edge block alone, then padded tails)
+    for i in range(0, 64, 7):
+        full_parity(data[128 * i: 128 * i + 128], ew)
+
+
+@pytest.mark.parametrize("ew", [4, 2, 1, 8])
+def test_tiny_alphabet_multi_chunk(ew):
+    dt = "bf16" if ew == 2 else "fp32"
+    full_parity(W.tiny_alphabet_blocks(32 * 70 + 5, dt, seed=ew), ew)
+
+
+@pytest.mark.parametrize("ew", [4, 2])
+def test_tail_sizes(ew):
+    rng = np.random.default_rng(21)
+    for n in W.TAIL_SIZES + (4096 * 3 + 130, 4096 * 5 - 2):
+        for data in (bytes(n), rng.integers(0, 256, n, dtype=np.uint8).tobytes(),
+                     W.relu_values(n // 4 + 1, rng).tobytes()[:n],
+                     W.f32_to_bf16_rne(W.gelu_values(n // 2 + 1, rng)).tobytes()[:n]):
+            if n == 0:
+                got = gpu_compress(data, ew)
+                assert got == b"" and oracle.compress(data, ew) == b""
+                st, back = gpu_decompress(b"", 0, ew)
+                assert st == 0
+                continue
+            full_parity(data, ew)
+
+
+def test_random_and_zero_chunks():
+    rng = np.random.default_rng(22)
+    data = np.concatenate([np.zeros(4096 * 3, np.uint8), rng.integers(0, 256, 4096 * 3, dtype=np.uint8),
+                           np.zeros(100, np.uint8)])
+    for ew in (4, 2):
+        s = full_parity(data, ew)
+        lens, _ = chunk_table(s, data.size)
+        assert list(lens[3:6]) == [4096] * 3
+
+
+# ------------------------------------------------------ workload configs
+
+def test_config1_relu_fp32_4mib_full():
+    t = W.relu_fp32_4mib()
+    s = full_parity(t.data, 4)
+    assert t.nbytes / len(s) > 1.5
+
+
+def test_config2_conv_bf16_full():
+    t = W.conv_bf16()
+    s = full_parity(t.data, 2)
+    assert t.nbytes / len(s) > 1.5
+
+
+def _large_case(t, nsample=48, seed=0):
+    x = to_device(t.data)
+    out, total = gpu_compress_dev(x, t.elem_width)
+    C = (t.nbytes + 4095) // 4096
+    hdr = out[: 2 * C].cpu().numpy().view("<u2").astype(np.int64)
+    assert total == 2 * C + int(hdr.sum())
+    raw_lens = np.minimum(4096, t.nbytes - 4096 * np.arange(C))
+    assert (hdr >= 1).all() and (hdr <= raw_lens).all()
+    stream = out[:total].cpu().numpy().tobytes()
+    rng = np.random.default_rng(seed)
+    chunks = sorted(set([0, 1, C - 1] + rng.integers(0, C, nsample).tolist()))
+    sampled_chunk_parity(t.data, t.elem_width, stream, chunks)
+    back, st = _lib.decompress_tensor(out, total, t.elem_width, t.nbytes)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(back[: t.nbytes], x)
+    return total
+
+
+def test_config3_attention_bf16_sampled():
+    t = W.attention_bf16()
+    total = _large_case(t)
+    assert t.nbytes / total > 1.5
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_config4_mlp_ln_sampled(dtype):
+    for t in W.mlp_ln(dtype=dtype):
+        _large_case(t, seed=3)
+
+
+@pytest.mark.parametrize("seg", list(range(len(W.SWEEP_SEGMENTS))))
+def test_config5_sweep_segments_sampled(seg):
+    kind, dt = W.SWEEP_SEGMENTS[seg]
+    _large_case(W.sweep_segment(kind, dt), seed=seg)
+
+
+# ----------------------------------------------------------- decoder only
+
+def test_decodes_oracle_streams():
+    t = W.relu_fp32_4mib()
+    s = oracle.compress(t.data, 4)
+    st, back = gpu_decompress(s, t.nbytes, 4)
+    assert st == 0 and back == t.data.tobytes()
+    t2 = W.conv_bf16()
+    s2 = oracle.compress(t2.data, 2)
+    st, back = gpu_decompress(s2, t2.nbytes, 2)
+    assert st == 0 and back == t2.data.tobytes()
+
+
+def test_corrupt_streams_report_status():
+    rng = np.random.default_rng(23)
+    data = W.relu_values(4 * 1024 + 300, rng).tobytes()
+    n = len(data)
+    s = bytearray(oracle.compress(data, 4))
+    C = (n + 4095) // 4096
+    bad = bytearray(s); bad[0:2] = (0).to_bytes(2, "little")
+    assert gpu_decompress(bytes(bad), n, 4)[0] == _lib.PZ_ERR_CORRUPT
+    bad = bytearray(s); bad[0:2] = (4097).to_bytes(2, "little")
+    assert gpu_decompress(bytes(bad), n, 4)[0] == _lib.PZ_ERR_CORRUPT
+    assert gpu_decompress(bytes(s), n, 4, comp_bytes=len(s) - 1)[0] == _lib.PZ_ERR_CORRUPT
+    bad = bytearray(s); bad[2 * C] = (bad[2 * C] & ~7) | 6          # tag 6
+    assert gpu_decompress(bytes(bad), n, 4)[0] == _lib.PZ_ERR_CORRUPT
+    for _ in range(200):
+        bad = bytearray(s)
+        pos = int(rng.integers(16 * 8, len(bad) * 8))
+        bad[pos // 8] ^= 1 << (pos % 8)
+        st, out = gpu_decompress(bytes(bad), n, 4)
+        rc_ref, out_ref = oracle.decompress_status(bytes(bad), n, 4)
+        assert st in (_lib.PZ_OK, _lib.PZ_ERR_CORRUPT)
+        assert st == rc_ref
+        if st == 0:
+            assert out == out_ref
+
+
+def test_repeated_calls_and_streams_are_deterministic():
+    t = W.relu_fp32_4mib()
+    x = to_device(t.data)
+    ref = None
+    s2 = torch.cuda.Stream()
+    for i in range(4):
+        with torch.cuda.stream(s2 if i % 2 else torch.cuda.current_stream()):
+            out, total = _lib.compress_tensor(x, 4)
+        torch.cuda.synchronize()
+        got = out[: int(total.item())].cpu()
+        if ref is None:
+            ref = got
+        assert torch.equal(got, ref)
