@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark of the PlaneZip block codec on GB300: raw-byte GB/s of compress
+and decompress through the C ABI, the compression ratio, and the roofline
+fraction of the dominant kernel, on the 1 GiB throughput sweep.
+
+One step = every segment of the sweep compressed (one pz_compress call per
+segment) and then decompressed (one pz_decompress call per segment), back to
+back on one stream, inputs resident in HBM. Each segment (128-256 MiB) is
+larger than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica on its own GPU (the codec has no exchange step); the
+step time is the maximum over ranks and `value` counts all ranks' bytes.
+`--impl reference` times the CPU oracle (the only reference this codec has)
+on a bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "raw-byte GB/s compress & decompress (BF16/FP32) vs HBM roofline; ratio"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("1 GiB throughput sweep: {ReLU, smooth conv, causal attention} x {FP32, BF16} "
+            "at 128 MiB each + 256 MiB uniform u32; one compress call per segment, then all "
+            "segments decompressed, back to back on one stream")
+
+# DRAM bytes per launch of the dominant kernel from one ncu capture
+# (profiles/ summary named for the kernel and workload). None until a capture
+# of the current kernel exists.
+NCU_TRAFFIC_BYTES_PER_LAUNCH = None
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-sample-mib", type=float, default=4.0,
+                    help="MiB per segment timed through the CPU oracle")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workload
+
+def make_workload():
+    from lossless_bit_plane_gb300 import workloads as W
+
+    return W.sweep_1gib()
+
+
+def peak_hbm():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(segs, mib: float):
+    """Round trip of the first `mib` MiB of every segment through the oracle
+    (single thread); returns (raw bytes, compress s, decompress s)."""
+    import oracle
+
+    oracle.build()
+    nb, tc, td = 0, 0.0, 0.0
+    for t in segs:
+        n = min(t.nbytes, int(mib * (1 << 20)))
+        piece = t.data[:n]
+        t0 = time.perf_counter()
+        s = oracle.compress(piece, t.elem_width)
+        t1 = time.perf_counter()
+        back = oracle.decompress(s, n, t.elem_width)
+        t2 = time.perf_counter()
+        assert back == piece.tobytes()
+        nb += n
+        tc += t1 - t0
+        td += t2 - t1
+    return nb, tc, td
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return 0
+    segs = make_workload()
+    mib = min(args.cpu_sample_mib, 1.0)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(segs, mib)
+    nb_tot, tc_tot, td_tot = 0, 0.0, 0.0
+    for _ in range(args.steps):
+        nb, tc, td = cpu_oracle_sample(segs, mib)
+        nb_tot += nb
+        tc_tot += tc
+        td_tot += td
+    value = nb_tot / (tc_tot + td_tot) / 1e9
+    sample = f"first {mib:g} MiB of each of the {len(segs)} sweep segments per step, compress + decompress"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (tc_tot + td_tot) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "compress_gbs": nb_tot / tc_tot / 1e9, "decompress_gbs": nb_tot / td_tot / 1e9,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- GPU
+
+def run_ours(args, rank: int, world: int, local: int):
+    import torch
+
+    from lossless_bit_plane_gb300 import _lib, build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    build.build()
+    _lib.load()
+
+    segs = make_workload()
+    stream = torch.cuda.current_stream(dev)
+    d_in = [torch.from_numpy(t.data).to(dev) for t in segs]
+    d_out = [torch.empty(_lib.pz_max_compressed_bytes(t.nbytes), dtype=torch.uint8, device=dev) for t in segs]
+    d_tot = torch.zeros(len(segs), dtype=torch.int64, device=dev)
+    d_back = [torch.empty(t.nbytes, dtype=torch.uint8, device=dev) for t in segs]
+    d_st = torch.zeros(len(segs), dtype=torch.int32, device=dev)
+    sh = stream.cuda_stream
+
+    def compress_all(evs=None):
+        for i, t in enumerate(segs):
+            if evs:
+                evs[i][0].record(stream)
+            rc = _lib.pz_compress(d_in[i].data_ptr(), t.nbytes, t.elem_width, d_out[i].data_ptr(), d_out[i].numel(),
+                                  d_tot[i:i + 1].data_ptr(), sh)
+            assert rc == 0, rc
+            if evs:
+                evs[i][1].record(stream)
+
+    totals_host = None
+
+    def decompress_all(totals, evs=None):
+        for i, t in enumerate(segs):
+            if evs:
+                evs[i][0].record(stream)
+            rc = _lib.pz_decompress(d_out[i].data_ptr(), int(totals[i]), t.elem_width, d_back[i].data_ptr(), t.nbytes,
+                                    d_st[i:i + 1].data_ptr(), sh)
+            assert rc == 0, rc
+            if evs:
+                evs[i][1].record(stream)
+
+    # first pass: totals (the decompressor's comp_bytes) and a correctness check
+    compress_all()
+    torch.cuda.synchronize()
+    totals_host = d_tot.cpu().tolist()
+    decompress_all(totals_host)
+    torch.cuda.synchronize()
+    assert d_st.cpu().tolist() == [0] * len(segs)
+    for i in range(len(segs)):
+        assert torch.equal(d_back[i], d_in[i]), f"round trip failed on segment {i}"
+
+    for _ in range(args.warmup):
+        compress_all()
+        decompress_all(totals_host)
+    torch.cuda.synchronize()
+
+    nseg = len(segs)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    c_evs = [[[ev(), ev()] for _ in range(nseg)] for _ in range(args.steps)]
+    d_evs = [[[ev(), ev()] for _ in range(nseg)] for _ in range(args.steps)]
+    start, stop = ev(), ev()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        compress_all(c_evs[k])
+        decompress_all(totals_host, d_evs[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop() if clocks else None
+    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(dist, elapsed_ms, dev)
+
+    totals_now = d_tot.cpu().tolist()
+    assert totals_now == totals_host
+    raw = sum(t.nbytes for t in segs)
+    comp = sum(totals_host)
+    t_c = [sum(c_evs[k][i][0].elapsed_time(c_evs[k][i][1]) for k in range(args.steps)) / args.steps for i in range(nseg)]
+    t_d = [sum(d_evs[k][i][0].elapsed_time(d_evs[k][i][1]) for k in range(args.steps)) / args.steps for i in range(nseg)]
+    tc_ms, td_ms = sum(t_c), sum(t_d)
+    peak, peak_kind = peak_hbm()
+    # algorithmic bytes per call: raw read + stream written (compress),
+    # stream read + raw written (decompress); both are raw + stream
+    alg = [t.nbytes + totals_host[i] for i, t in enumerate(segs)]
+    comp_ach = sum(alg) / (tc_ms * 1e-3) / 1e9
+    dec_ach = sum(alg) / (td_ms * 1e-3) / 1e9
+    dominant = "pz_encode" if tc_ms >= td_ms else "pz_decode"
+    ach = comp_ach if dominant == "pz_encode" else dec_ach
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, segs, d_out, d_back, d_tot, d_st, totals_host, dev, stream, world, dist)
+
+    per_seg = []
+    for i, t in enumerate(segs):
+        per_seg.append({"segment": t.name, "elem_width": t.elem_width, "bytes": t.nbytes,
+                        "ratio": round(t.nbytes / totals_host[i], 4),
+                        "compress_gbs": round(t.nbytes / (t_c[i] * 1e-3) / 1e9, 1),
+                        "decompress_gbs": round(t.nbytes / (t_d[i] * 1e-3) / 1e9, 1),
+                        "compress_roofline_frac": round(alg[i] / (t_c[i] * 1e-3) / 1e9 / peak, 3),
+                        "decompress_roofline_frac": round(alg[i] / (t_d[i] * 1e-3) / 1e9 / peak, 3)})
+
+    cpu = None
+    if rank == 0:
+        nb, tcpu_c, tcpu_d = cpu_oracle_sample(segs, args.cpu_sample_mib)
+        cpu = {"value": nb / (tcpu_c + tcpu_d) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {args.cpu_sample_mib:g} MiB of each of the {nseg} sweep segments, compress + "
+                         f"decompress, single thread",
+               "compress_gbs": nb / tcpu_c / 1e9, "decompress_gbs": nb / tcpu_d / 1e9}
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * raw / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "bytes_per_step_per_gpu": raw, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (128-256 MiB per call); no flush",
+                   "sha256": {t.name: __import__("lossless_bit_plane_gb300.workloads", fromlist=["x"]).sha256(t.data)[:16]
+                              for t in segs}},
+        "compress_gbs": world * raw / (tc_ms * 1e-3) / 1e9,
+        "decompress_gbs": world * raw / (td_ms * 1e-3) / 1e9,
+        "ratio": raw / comp,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "peak_kind": peak_kind,
+                     "traffic": NCU_TRAFFIC_BYTES_PER_LAUNCH,
+                     "encode_frac": comp_ach / peak, "decode_frac": dec_ach / peak},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * nseg * args.steps,
+        "clocks": clk,
+        "segments": per_seg,
+        "eq2": eq2(raw / comp, raw / (tc_ms * 1e-3) / 1e9),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, segs, d_out, d_back, d_tot, d_st, totals_host, dev, stream, world, dist):
+    """Same round trip through the C ABI, but every step copies each segment's
+    input from pinned host memory to the device first and reads the
+    compressed sizes and decode statuses back to the host at the end."""
+    import torch
+
+    from lossless_bit_plane_gb300 import _lib
+
+    h_in = [torch.from_numpy(t.data).pin_memory() for t in segs]
+    d_in = [torch.empty(t.nbytes, dtype=torch.uint8, device=dev) for t in segs]
+    h_res = torch.empty(2 * len(segs), dtype=torch.int64).pin_memory()
+    sh = stream.cuda_stream
+
+    def step():
+        for i, t in enumerate(segs):
+            d_in[i].copy_(h_in[i], non_blocking=True)
+            rc = _lib.pz_compress(d_in[i].data_ptr(), t.nbytes, t.elem_width, d_out[i].data_ptr(), d_out[i].numel(),
+                                  d_tot[i:i + 1].data_ptr(), sh)
+            assert rc == 0
+        for i, t in enumerate(segs):
+            rc = _lib.pz_decompress(d_out[i].data_ptr(), int(totals_host[i]), t.elem_width, d_back[i].data_ptr(),
+                                    t.nbytes, d_st[i:i + 1].data_ptr(), sh)
+            assert rc == 0
+        h_res[: len(segs)].copy_(d_tot, non_blocking=True)
+        h_res[len(segs):].copy_(d_st.to(torch.int64), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(dist, t0.elapsed_time(t1) / args.steps, dev)
+    assert h_res[: len(segs)].tolist() == totals_host and h_res[len(segs):].tolist() == [0] * len(segs)
+    raw = sum(t.nbytes for t in segs)
+    return {"value": world * raw / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": raw, "d2h_bytes_per_step": 16 * len(segs)}
+
+
+def eq2(ratio: float, bce_gbs: float, gammas=(24.0, 450.0)):
+    """The paper's effective transfer time x_t = min(m/g, max(m/(c g), m/B_CE))
+    (Section III-C, Eq. 2) per GiB, for the measured ratio c and compress rate
+    B_CE, at the paper's PCIe 4.0 24 GB/s and at an assumed 450 GB/s per
+    direction for GB300's NVLink-C2C host link."""
+    m = float(1 << 30)
+    out = {}
+    for g in gammas:
+        x = min(m / (g * 1e9), max(m / (ratio * g * 1e9), m / (bce_gbs * 1e9)))
+        out[f"gamma_{g:g}GBps"] = {"x_t_ms_per_GiB": 1e3 * x, "uncompressed_ms_per_GiB": 1e3 * m / (g * 1e9)}
+    return out
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

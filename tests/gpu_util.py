@@ -10,7 +10,7 @@ from lossless_bit_plane_gb300 import _lib
 
 
 def to_device(data) -> torch.Tensor:
-    arr = np.frombuffer(bytes(data), dtype=np.uint8) if not isinstance(data, np.ndarray) else data.view(np.uint8).reshape(-1)
+    arr = np.frombuffer(bytes(data), dtype=np.uint8).copy() if not isinstance(data, np.ndarray) else data.view(np.uint8).reshape(-1)
     x = torch.empty(arr.size, dtype=torch.uint8, device="cuda")
     if arr.size:
         x.copy_(torch.from_numpy(np.ascontiguousarray(arr)))
