@@ -104,209 +104,186 @@ __device__ __forceinline__ uint32_t lds16d(uint32_t addr) {
 __device__ __forceinline__ void sts32d(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t scr(uint32_t row, uint32_t word, uint32_t lane) {
+__device__ __forceinline__ void sts16d(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
+}
+// Lane-private 32-word row, XOR-swizzled by lane (conflict-free across lanes).
+__device__ __forceinline__ uint32_t prow(uint32_t row, uint32_t lane, uint32_t word) {
   return row + (((word ^ lane) & 31u) << 2);
 }
+__device__ __forceinline__ uint32_t prow_half(uint32_t row, uint32_t lane, uint32_t h) {
+  return prow(row, lane, h >> 1) + ((h & 1u) << 1);
+}
 
-// Parse the plane codes of one block, top plane first, into pre-XOR planes.
-// T is uint32_t (planes up to 32 bits) or uint64_t (up to 64). rows receives
-// plane i for i < 32 (T = u32) or i < 16 (T = u64, low and high words in
-// rows[i] and rows[16 + i]). Returns false on a malformed code.
-template <typename T, int MAXTOP>
-__device__ __forceinline__ bool parse_planes(BitReader &br, int top, int W, int p, int K,
-                                             T (&P)[MAXTOP + 1]) {
-  const T full = (W >= (int)(8 * sizeof(T))) ? ~(T)0 : (((T)1 << W) - 1);
-  T Pup = 0;
+// Parse the P = top+1 plane codes of one block, top plane first, rebuilding
+// the pre-XOR planes P_i = X_i ^ P_{i+1}, and store them in the lane's row:
+// FP32 plane i < 32 in word i; BF16 plane i < 16 in words i (symbols 0..31)
+// and 16+i (symbols 32..63). For DBX the rows are pre-shifted so that row
+// bit j holds delta j (plane bit q is delta q+1); the top DBX plane (the
+// borrow plane) is not stored. Returns false on a malformed code.
+template <bool W16>
+__device__ __forceinline__ bool parse_plane_rows(BitReader &br, uint32_t row, uint32_t lane, int top, int W,
+                                                 int p, bool dbx) {
+  const int K = W16 ? 4 : 5;
+  const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
+  uint64_t Pup = 0;
   int run = 0;
-  bool ok = true;
-#pragma unroll
-  for (int i = MAXTOP; i >= 0; --i) {
-    if (i > top) {
-      P[i] = 0;
-      continue;
-    }
-    T X = 0;
+#pragma unroll 1
+  for (int i = top; i >= 0; --i) {
+    uint64_t X = 0;
     if (run > 0) {
       --run;
     } else {
       br.ensure(16);
-      uint32_t v = br.peek(16);
-      if (v & 1u) {
+      const uint32_t v = br.peek(16);
+      if (v & 1u) {  // 1 + plane
         br.skip(1);
-        X = (T)br.get64((uint32_t)W);
-      } else if ((v & 3u) == 2u) {
-        int L = 2 + (int)((v >> 2) & ((1u << K) - 1));
+        X = br.get64((uint32_t)W);
+      } else if ((v & 3u) == 2u) {  // 0 1 + (run - 2)
+        const int L = 2 + (int)((v >> 2) & ((1u << K) - 1));
         br.skip(2 + K);
-        if (L > i + 1) ok = false;
+        if (L > i + 1) return false;
         run = L - 1;
-      } else if ((v & 7u) == 4u) {
+      } else if ((v & 7u) == 4u) {  // 0 0 1
         br.skip(3);
       } else {
-        uint32_t code = v & 31u;
+        const uint32_t code = v & 31u;
         br.skip(5);
-        if (code == 0) {
+        if (code == 0) {  // 0 0 0 0 0: all ones
           X = full;
-        } else if (code == 16) {
-          if (i == top) ok = false;
+        } else if (code == 16) {  // 0 0 0 0 1: pre-XOR plane zero
+          if (i == top) return false;
           X = Pup;
-        } else {
-          uint32_t q = br.get((uint32_t)p);
+        } else {  // 0 0 0 1 0 / 0 0 0 1 1 + q
+          const int q = (int)br.get((uint32_t)p);
           if (code == 8) {
-            if ((int)q + 1 >= W) ok = false;
-            else X = (T)3 << q;
+            if (q + 1 >= W) return false;
+            X = 3ull << q;
           } else {
-            if ((int)q >= W) ok = false;
-            else X = (T)1 << q;
+            if (q >= W) return false;
+            X = 1ull << q;
           }
         }
       }
     }
-    T Pi = (i == top) ? X : (T)(X ^ Pup);
-    P[i] = Pi;
+    const uint64_t Pi = (i == top) ? X : (X ^ Pup);
     Pup = Pi;
-  }
-  return ok;
-}
-
-// ---------------------------------------------------------------- FP32
-__device__ __forceinline__ bool decode_block32(BitReader &br, uint32_t (&s)[32], uint32_t row,
-                                               uint32_t lane) {
-  const uint32_t tag = br.get(3);
-  if (tag == kTagZVC) {
-    const uint32_t mask = br.get(32);
-#pragma unroll
-    for (int k = 0; k < 32; ++k) s[k] = ((mask >> k) & 1u) ? br.get(32) : 0u;
-    return true;
-  }
-  if (tag == kTagRAW) {
-#pragma unroll
-    for (int k = 0; k < 32; ++k) s[k] = br.get(32);
-    return true;
-  }
-  if (tag > kTagRAW) return false;
-  uint32_t basesym = 0, mask = 0;
-  int top = 31, W = 32;
-  if (tag == kTagDBX) {
-    basesym = br.get(32);
-    top = 32;
-    W = 31;
-  } else if (tag == kTagZBX) {
-    mask = br.get(32);
-    W = __popc(mask);
-    if (W == 0) {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) s[k] = 0;
-      return true;
+    if (W16) {
+      if (i < 16) {
+        sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
+        sts32d(prow(row, lane, (uint32_t)i + 16), dbx ? (uint32_t)(Pi >> 31) : (uint32_t)(Pi >> 32));
+      }
+    } else {
+      if (i < 32) sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
     }
   }
-  uint32_t P[33];
-  bool ok = parse_planes<uint32_t, 32>(br, top, W, ceil_log2_int(W), 5, P);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) s[i] = (tag == kTagDBX) ? (P[i] << 1) : P[i];
-  transpose32(s);
-  if (tag == kTagDBX) {
-    s[0] = basesym;
-#pragma unroll
-    for (int j = 1; j < 32; ++j) s[j] += s[j - 1];
-  } else if (tag == kTagZBX) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < W) sts32d(scr(row, j, lane), s[j]);
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      uint32_t rank = __popc(mask & ((1u << k) - 1u));
-      s[k] = ((mask >> k) & 1u) ? lds32d(scr(row, rank, lane)) : 0u;
-    }
-  }
-  return ok;
+  return true;
 }
 
-// ---------------------------------------------------------------- BF16
-// Produces the split-packed block (word j = symbol j | symbol j+32 << 16).
-__device__ __forceinline__ bool decode_block16(BitReader &br, uint32_t (&sp)[32], uint32_t row,
-                                               uint32_t lane) {
+// Decode one block into o[32], the block's 32 words in memory order.
+template <bool W16>
+__device__ __forceinline__ bool decode_block(BitReader &br, uint32_t (&o)[32], uint32_t row, uint32_t lane) {
   const uint32_t tag = br.get(3);
-  if (tag == kTagZVC) {
-    const uint32_t mlo = br.get(32), mhi = br.get(32);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) sp[j] = ((mlo >> j) & 1u) ? br.get(16) : 0u;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if ((mhi >> j) & 1u) sp[j] |= br.get(16) << 16;
-    return true;
-  }
-  if (tag == kTagRAW) {
-    uint32_t raw[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) raw[r] = br.get(32);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) sp[j] = split_word(raw, j);
-    return true;
-  }
   if (tag > kTagRAW) return false;
+  if (tag == kTagRAW) {
+#pragma unroll 4
+    for (uint32_t k = 0; k < 32; ++k) sts32d(prow(row, lane, k), br.get(32));
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = lds32d(prow(row, lane, k));
+    return true;
+  }
+  if (tag == kTagZVC) {
+    if (W16) {
+      const uint32_t mlo = br.get(32), mhi = br.get(32);
+#pragma unroll 1
+      for (uint32_t h = 0; h < 64; ++h) {
+        const uint32_t bit = (h < 32) ? (mlo >> h) : (mhi >> (h - 32));
+        sts16d(prow_half(row, lane, h), (bit & 1u) ? br.get(16) : 0u);
+      }
+    } else {
+      const uint32_t mask = br.get(32);
+#pragma unroll 1
+      for (uint32_t k = 0; k < 32; ++k) sts32d(prow(row, lane, k), ((mask >> k) & 1u) ? br.get(32) : 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = lds32d(prow(row, lane, k));
+    return true;
+  }
   uint32_t basesym = 0, mlo = 0, mhi = 0;
-  int top = 15, W = 64;
+  int top = W16 ? 15 : 31, W = W16 ? 64 : 32;
   if (tag == kTagDBX) {
-    basesym = br.get(16);
-    top = 16;
-    W = 63;
+    basesym = br.get(W16 ? 16 : 32);
+    ++top;
+    --W;
   } else if (tag == kTagZBX) {
     mlo = br.get(32);
-    mhi = br.get(32);
+    if (W16) mhi = br.get(32);
     W = __popc(mlo) + __popc(mhi);
     if (W == 0) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) sp[j] = 0;
+      for (int k = 0; k < 32; ++k) o[k] = 0;
       return true;
     }
   }
-  uint64_t P[17];
-  bool ok = parse_planes<uint64_t, 16>(br, top, W, ceil_log2_int(W), 4, P);
+  if (!parse_plane_rows<W16>(br, row, lane, top, W, ceil_log2_int(W), tag == kTagDBX)) return false;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if (tag == kTagDBX) {  // plane bit q is delta q+1: lanes j>=1 low, j+32 high
-      sp[i] = (uint32_t)(P[i] << 1);
-      sp[16 + i] = (uint32_t)(P[i] >> 31);
-    } else {
-      sp[i] = (uint32_t)P[i];
-      sp[16 + i] = (uint32_t)(P[i] >> 32);
+  for (int j = 0; j < 32; ++j) o[j] = lds32d(prow(row, lane, j));
+  transpose32(o);  // FP32: o[j] = symbol j (or delta j); BF16: split words
+  if (!W16) {
+    if (tag == kTagDBX) {
+      o[0] = basesym;
+#pragma unroll
+      for (int j = 1; j < 32; ++j) o[j] += o[j - 1];
+    } else if (tag == kTagZBX) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < W) sts32d(prow(row, lane, j), o[j]);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const uint32_t rank = __popc(mlo & ((1u << k) - 1u));
+        o[k] = ((mlo >> k) & 1u) ? lds32d(prow(row, lane, rank)) : 0u;
+      }
     }
+    return true;
   }
-  transpose32(sp);
+  // BF16: o holds split words (word j = symbol j | symbol j+32 << 16)
   if (tag == kTagDBX) {
     uint32_t prev = basesym;  // s_0
-    sp[0] = (sp[0] & 0xFFFF0000u) | prev;
+    o[0] = (o[0] & 0xFFFF0000u) | prev;
 #pragma unroll
     for (int j = 1; j < 32; ++j) {  // s_j = s_{j-1} + d_j
-      prev = (prev + sp[j]) & 0xFFFFu;
-      sp[j] = (sp[j] & 0xFFFF0000u) | prev;
+      prev = (prev + o[j]) & 0xFFFFu;
+      o[j] = (o[j] & 0xFFFF0000u) | prev;
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {  // s_{j+32} = s_{j+31} + d_{j+32}
-      prev = (prev + (sp[j] >> 16)) & 0xFFFFu;
-      sp[j] = (sp[j] & 0xFFFFu) | (prev << 16);
+      prev = (prev + (o[j] >> 16)) & 0xFFFFu;
+      o[j] = (o[j] & 0xFFFFu) | (prev << 16);
     }
   } else if (tag == kTagZBX) {
-    // survivors t_0..t_{W-1} are sp[j] low (t_j) and high (t_{j+32}); store
-    // them as half-words in index order, then gather by rank
+    // survivors t_0..t_{W-1}: t_j in o[j] low, t_{j+32} in o[j] high; store
+    // them as half-words in index order, then gather each symbol by rank
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      uint32_t lo = sp[j] & 0xFFFFu, hi = sp[j] >> 16;
-      // half-word h lives at word (h >> 1), half (h & 1)
-      if (j < W) asm volatile("st.shared.u16 [%0], %1;" ::"r"(scr(row, (uint32_t)j >> 1, lane) + ((j & 1) << 1)), "h"((unsigned short)lo) : "memory");
-      if (j + 32 < W) asm volatile("st.shared.u16 [%0], %1;" ::"r"(scr(row, (uint32_t)(j + 32) >> 1, lane) + ((j & 1) << 1)), "h"((unsigned short)hi) : "memory");
+      if (j < W) sts16d(prow_half(row, lane, j), o[j] & 0xFFFFu);
+      if (j + 32 < W) sts16d(prow_half(row, lane, j + 32), o[j] >> 16);
     }
     const uint32_t clo = __popc(mlo);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      uint32_t rl = __popc(mlo & ((1u << j) - 1u));
-      uint32_t rh = clo + __popc(mhi & ((1u << j) - 1u));
-      uint32_t vl = ((mlo >> j) & 1u) ? lds16d(scr(row, rl >> 1, lane) + ((rl & 1u) << 1)) : 0u;
-      uint32_t vh = ((mhi >> j) & 1u) ? lds16d(scr(row, rh >> 1, lane) + ((rh & 1u) << 1)) : 0u;
-      sp[j] = vl | (vh << 16);
+      const uint32_t rl = __popc(mlo & ((1u << j) - 1u));
+      const uint32_t rh = clo + __popc(mhi & ((1u << j) - 1u));
+      const uint32_t vl = ((mlo >> j) & 1u) ? lds16d(prow_half(row, lane, rl)) : 0u;
+      const uint32_t vh = ((mhi >> j) & 1u) ? lds16d(prow_half(row, lane, rh)) : 0u;
+      o[j] = vl | (vh << 16);
     }
   }
-  return ok;
+  uint32_t sp[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) sp[j] = o[j];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) o[r] = raw_word_from_split(sp, r);
+  return true;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -398,16 +375,9 @@ __global__ void __launch_bounds__(kDecWarps * 32)
     bool ok = true;
     for (uint32_t b = 0; b < nblk && ok; ++b) {
       uint32_t s[32];
-      ok = W16 ? decode_block16(br, s, row, lane) : decode_block32(br, s, row, lane);
+      ok = decode_block<W16>(br, s, row, lane);
       if (br.consumed > 8ull * L) ok = false;
       if (!ok) break;
-      if (W16) {
-        uint32_t sp[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sp[j] = s[j];
-#pragma unroll
-        for (int r = 0; r < 32; ++r) s[r] = raw_word_from_split(sp, r);
-      }
       uint8_t *bd = dst + 128u * b;
       const uint32_t take = min(128u, raw_len - 128u * b);
       if (take == 128u) {

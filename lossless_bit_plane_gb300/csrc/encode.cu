@@ -85,6 +85,7 @@ __device__ __forceinline__ int single_plane_len(T X, T full, int W, int p) {
 
 struct Sizes {
   int s[5];
+  uint32_t m0, m1;  // non-zero symbol masks: symbols 0..31 and (BF16) 32..63
 };
 
 __device__ __forceinline__ void select_min(const Sizes &z, uint32_t &tag, uint32_t &bits) {
@@ -136,6 +137,8 @@ __device__ __forceinline__ Sizes classify32(const uint32_t (&s)[32]) {
     }
   }
   Sizes z;
+  z.m0 = nz;
+  z.m1 = 0;
   int n = __popc(nz);
   z.s[kTagZVC] = 32 + 32 * n;
   z.s[kTagRAW] = 1024;
@@ -217,6 +220,8 @@ __device__ __forceinline__ Sizes classify16(const uint32_t (&sp)[32]) {
   auto lo = [](uint32_t v) { return v & 0xFFFFu; };
   auto hi = [](uint32_t v) { return v >> 16; };
   Sizes z;
+  z.m0 = mlo;
+  z.m1 = mhi;
   int n = __popc(mlo) + __popc(mhi);
   z.s[kTagZVC] = 64 + 16 * n;
   z.s[kTagRAW] = 1024;
@@ -259,70 +264,19 @@ __device__ __forceinline__ Sizes classify16(const uint32_t (&sp)[32]) {
 }
 
 // ------------------------------------------------------------------ emit
+// Emission works out of the lane's own 128-byte row of the stage: first the
+// block's words as the TMA left them (128-byte swizzle), later the lane's 32
+// transposed plane rows (XOR-swizzled by lane). Per-plane work runs as short
+// runtime loops over that row so that the kernel's code stays small.
 
-__device__ __forceinline__ void emit_run(BitWriter &bw, int run, int K) {
-  if (run == 1)
-    bw.put(4u, 3);  // 0 0 1
-  else
-    bw.put(2u | ((uint32_t)(run - 2) << 2), 2 + K);  // 0 1 + (run-2)
+__device__ __forceinline__ uint32_t stage_word(uint32_t rowbase, uint32_t r, uint32_t k) {
+  return rowbase + ((((k >> 2) ^ (r & 7u)) << 4) | ((k & 3u) << 2));
 }
-
-template <typename T>
-__device__ __forceinline__ void emit_plane(BitWriter &bw, T X, bool prexor_zero, int W, int p,
-                                           T full) {
-  int ones = (sizeof(T) == 8) ? __popcll((uint64_t)X) : __popc((uint32_t)X);
-  int q = (sizeof(T) == 8) ? (__ffsll((long long)X) - 1) : (__ffs((int)X) - 1);
-  bool A = (X == full);
-  bool T2 = (ones == 2) && ((X >> q) == (T)3);
-  bool S1 = (ones == 1);
-  int best = 1 + W, code = 4;
-  if (S1 && 5 + p <= best) { best = 5 + p; code = 3; }
-  if (T2 && 5 + p <= best) { best = 5 + p; code = 2; }
-  if (prexor_zero && 5 <= best) { best = 5; code = 1; }
-  if (A && 5 <= best) { best = 5; code = 0; }
-  switch (code) {
-    case 0: bw.put(0u, 5); break;                                    // 0 0 0 0 0
-    case 1: bw.put(16u, 5); break;                                   // 0 0 0 0 1
-    case 2: bw.put(8u | ((uint32_t)q << 5), 5 + p); break;           // 0 0 0 1 0 + q
-    case 3: bw.put(24u | ((uint32_t)q << 5), 5 + p); break;          // 0 0 0 1 1 + q
-    default:
-      bw.put(1u, 1);                                                 // 1 + plane
-      bw.put64((uint64_t)X, (uint32_t)W);
-      break;
-  }
+__device__ __forceinline__ uint32_t stage_half(uint32_t rowbase, uint32_t r, uint32_t h) {
+  return stage_word(rowbase, r, h >> 1) + ((h & 1u) << 1);
 }
-
-// Emit P planes, top first. plane(i) returns X_i (bits >= W are zero).
-template <typename T, typename PlaneFn>
-__device__ __forceinline__ void emit_planes(BitWriter &bw, int top, int W, int p, int K,
-                                            PlaneFn plane) {
-  const T full = (W >= (int)(8 * sizeof(T))) ? ~(T)0 : (((T)1 << W) - 1);
-  int run = 0;
-  T Pup = 0;
-#pragma unroll
-  for (int i = 33; i >= 0; --i) {
-    if (i > top) continue;
-    T X = plane(i);
-    T P = (i == top) ? X : (T)(X ^ Pup);
-    if (X == 0) {
-      ++run;
-    } else {
-      if (run) {
-        emit_run(bw, run, K);
-        run = 0;
-      }
-      emit_plane<T>(bw, X, (i != top) && (P == 0), W, p, full);
-    }
-    Pup = P;
-  }
-  if (run) emit_run(bw, run, K);
-}
-
-// Thread-private compaction scratch: the lane's own 128-byte row of the stage
-// (no other lane reads it once the block is in registers), XOR-swizzled by
-// lane so that lanes at equal indices hit different banks.
-__device__ __forceinline__ uint32_t scratch_addr(uint32_t row, uint32_t word, uint32_t lane) {
-  return row + (((word ^ lane) & 31u) << 2);
+__device__ __forceinline__ uint32_t plane_row(uint32_t rowbase, uint32_t lane, uint32_t i) {
+  return rowbase + (((i ^ lane) & 31u) << 2);
 }
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -335,97 +289,179 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
-
-// FP32 emit of the chosen candidate (s is consumed).
-__device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t (&s)[32],
-                                      uint32_t row, uint32_t lane) {
-  if (tag == kTagRAW) {
-#pragma unroll
-    for (int k = 0; k < 32; ++k) bw.put(s[k], 32);
-    return;
-  }
-  if (tag == kTagZVC) {
-    uint32_t nz = 0;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) nz |= (s[k] ? 1u : 0u) << k;
-    bw.put(nz, 32);
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      if (s[k]) bw.put(s[k], 32);
-    return;
-  }
-  if (tag == kTagDBX) {
-    bw.put(s[0], 32);
-    uint32_t Bw = 0;
-#pragma unroll
-    for (int j = 31; j >= 1; --j) {
-      uint64_t d = (uint64_t)s[j] - (uint64_t)s[j - 1];
-      uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);
-      Bw |= hi & (1u << (j - 1));
-      s[j] = lo ^ __funnelshift_r(lo, hi, 1);
-    }
-    s[0] = 0;
-    transpose32(s);
-    emit_planes<uint32_t>(bw, 32, 31, 5, 5,
-                          [&](int i) { return (i == 32) ? Bw : (s[i & 31] >> 1); });
-    return;
-  }
-  int W = 32, p = 5;
-  if (tag == kTagZBX) {
-    uint32_t nz = 0, cnt = 0;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      nz |= (s[k] ? 1u : 0u) << k;
-      if (s[k]) {
-        sts32(scratch_addr(row, cnt, lane), s[k]);
-        ++cnt;
-      }
-    }
-    bw.put(nz, 32);
-    if (cnt == 0) return;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) s[j] = ((uint32_t)j < cnt) ? lds32(scratch_addr(row, j, lane)) : 0u;
-    W = (int)cnt;
-    p = ceil_log2_int(W);
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) s[j] ^= s[j] >> 1;
-  transpose32(s);
-  emit_planes<uint32_t>(bw, 31, W, p, 5, [&](int i) { return s[i & 31]; });
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
 }
 
-// BF16 emit of the chosen candidate (sp, split-packed, is consumed).
-__device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t (&sp)[32],
-                                      uint32_t row, uint32_t lane) {
+__device__ __forceinline__ void emit_run(BitWriter &bw, int run, int K) {
+  if (run == 1)
+    bw.put(4u, 3);  // 0 0 1
+  else
+    bw.put(2u | ((uint32_t)(run - 2) << 2), 2 + K);  // 0 1 + (run-2)
+}
+
+// One non-zero plane: the shortest applicable code, ties in the order
+// all-ones, pre-XOR-zero, two-adjacent, single-one, verbatim.
+__device__ __forceinline__ void emit_plane(BitWriter &bw, uint64_t X, bool prexor_zero, int W, int p,
+                                           uint64_t full) {
+  const int ones = __popcll(X);
+  const int q = __ffsll((long long)X) - 1;
+  const bool A = (X == full);
+  const bool T2 = (ones == 2) && ((X >> q) == 3ull);
+  const bool S1 = (ones == 1);
+  int len = 1 + W;
+  uint32_t val = 0;
+  bool verbatim = true;
+  if (S1 && 5 + p <= len) { len = 5 + p; val = 24u | ((uint32_t)q << 5); verbatim = false; }  // 0 0 0 1 1 + q
+  if (T2 && 5 + p <= len) { len = 5 + p; val = 8u | ((uint32_t)q << 5); verbatim = false; }   // 0 0 0 1 0 + q
+  if (prexor_zero && 5 <= len) { len = 5; val = 16u; verbatim = false; }                        // 0 0 0 0 1
+  if (A && 5 <= len) { len = 5; val = 0u; verbatim = false; }                                    // 0 0 0 0 0
+  if (verbatim) {
+    bw.put(1u, 1);  // 1 + the plane
+    bw.put64(X, (uint32_t)W);
+  } else {
+    bw.put(val, (uint32_t)len);
+  }
+}
+
+// Plane codes, top plane first. Plane i < 32 (FP32) or < 16 (BF16, low and
+// high 32 symbols in rows i and 16+i) comes from the transposed rows; for
+// DBX the rows hold deltas at bit j = delta index j, so plane bit q = delta
+// q+1 needs a shift, and the top plane (the borrow plane) is passed in topv.
+template <bool W16>
+__device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase, uint32_t lane, int top,
+                                               int W, int p, bool dbx, uint64_t topv) {
+  const int K = W16 ? 4 : 5;
+  const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
+  int run = 0;
+  uint64_t Pup = 0;
+#pragma unroll 1
+  for (int i = top; i >= 0; --i) {
+    uint64_t X;
+    if (dbx && i == top) {
+      X = topv;
+    } else {
+      const uint32_t lo = lds32(plane_row(rowbase, lane, (uint32_t)i));
+      if (W16) {
+        const uint32_t hi = lds32(plane_row(rowbase, lane, (uint32_t)i + 16));
+        X = dbx ? ((uint64_t)(lo >> 1) | ((uint64_t)hi << 31)) : ((uint64_t)lo | ((uint64_t)hi << 32));
+      } else {
+        X = dbx ? (uint64_t)(lo >> 1) : (uint64_t)lo;
+      }
+    }
+    const uint64_t P = (i == top) ? X : (X ^ Pup);
+    if (X == 0) {
+      ++run;
+    } else {
+      if (run) {
+        emit_run(bw, run, K);
+        run = 0;
+      }
+      emit_plane(bw, X, (i != top) && (P == 0), W, p, full);
+    }
+    Pup = P;
+  }
+  if (run) emit_run(bw, run, K);
+}
+
+// FP32 emit of the chosen candidate. s: the block's symbols; nz: non-zero mask.
+__device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, const uint32_t (&s)[32], uint32_t nz,
+                                      uint32_t rowbase, uint32_t lane) {
   if (tag == kTagRAW) {
-#pragma unroll
-    for (int r = 0; r < 32; ++r) bw.put(raw_word_from_split(sp, r), 32);
+#pragma unroll 4
+    for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
     return;
   }
-  uint32_t mlo = 0, mhi = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    uint32_t m = halfmask_nonzero(sp[j]);
-    mlo |= (m & 1u) << j;
-    mhi |= (m >> 31) << j;
-  }
+  if (tag == kTagZVC || tag == kTagZBX) bw.put(nz, 32);
   if (tag == kTagZVC) {
+    for (uint32_t m = nz; m; m &= m - 1) bw.put(lds32(stage_word(rowbase, lane, __ffs(m) - 1)), 32);
+    return;
+  }
+  uint32_t T[32];
+  uint64_t topv = 0;
+  int top = 31, W = 32;
+  if (tag == kTagZBX) {
+    if (nz == 0) return;
+    uint32_t cnt = 0;  // compact the survivors in place (cnt <= k)
+    for (uint32_t m = nz; m; m &= m - 1, ++cnt)
+      sts32(stage_word(rowbase, lane, cnt), lds32(stage_word(rowbase, lane, __ffs(m) - 1)));
+    W = (int)cnt;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t t = ((uint32_t)j < cnt) ? lds32(stage_word(rowbase, lane, j)) : 0u;
+      T[j] = t ^ (t >> 1);
+    }
+  } else if (tag == kTagDBX) {
+    bw.put(s[0], 32);
+    uint32_t Bw = 0;
+    T[0] = 0;
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {
+      const uint64_t d = (uint64_t)s[j] - (uint64_t)s[j - 1];
+      const uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);
+      Bw |= hi & (1u << (j - 1));
+      T[j] = lo ^ __funnelshift_r(lo, hi, 1);
+    }
+    topv = Bw;
+    top = 32;
+    W = 31;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) T[j] = s[j] ^ (s[j] >> 1);
+  }
+  transpose32(T);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) sts32(plane_row(rowbase, lane, i), T[i]);
+  emit_plane_codes<false>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv);
+}
+
+// BF16 emit of the chosen candidate. sp: split-packed symbols (word j =
+// symbol j | symbol j+32 << 16); mlo/mhi: non-zero masks of 0..31 / 32..63.
+__device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, const uint32_t (&sp)[32], uint32_t mlo,
+                                      uint32_t mhi, uint32_t rowbase, uint32_t lane) {
+  if (tag == kTagRAW) {
+#pragma unroll 4
+    for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
+    return;
+  }
+  if (tag == kTagZVC || tag == kTagZBX) {
     bw.put(mlo, 32);
     bw.put(mhi, 32);
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (sp[j] & 0xFFFFu) bw.put(sp[j] & 0xFFFFu, 16);
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (sp[j] >> 16) bw.put(sp[j] >> 16, 16);
+  }
+  if (tag == kTagZVC) {
+    for (uint32_t m = mlo; m; m &= m - 1) bw.put(lds16(stage_half(rowbase, lane, __ffs(m) - 1)), 16);
+    for (uint32_t m = mhi; m; m &= m - 1) bw.put(lds16(stage_half(rowbase, lane, 31 + __ffs(m))), 16);
     return;
   }
-  if (tag == kTagDBX) {
+  uint32_t T[32];
+  uint64_t topv = 0;
+  int top = 15, W = 64;
+  if (tag == kTagZBX) {
+    uint32_t cnt = 0;  // compact the survivors' half-words in place (cnt <= h)
+    for (uint32_t m = mlo; m; m &= m - 1, ++cnt)
+      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, __ffs(m) - 1)));
+    for (uint32_t m = mhi; m; m &= m - 1, ++cnt)
+      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, 31 + __ffs(m))));
+    if (cnt == 0) return;
+    W = (int)cnt;
+    uint32_t rw[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) rw[r] = lds32(stage_word(rowbase, lane, r));
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t keep =
+          (((uint32_t)j < cnt) ? 0x0000FFFFu : 0u) | (((uint32_t)j + 32 < cnt) ? 0xFFFF0000u : 0u);
+      const uint32_t t = split_word(rw, j) & keep;
+      T[j] = t ^ ((t >> 1) & 0x7FFF7FFFu);
+    }
+  } else if (tag == kTagDBX) {
     bw.put(sp[0] & 0xFFFFu, 16);
     const uint32_t s31lo = sp[31] << 16;
     uint32_t Blo = 0, Bhi = 0;
 #pragma unroll
-    for (int j = 31; j >= 0; --j) {
+    for (int j = 0; j < 32; ++j) {
       uint32_t bo;
       uint32_t d = sub16x2(sp[j], j ? sp[j - 1] : s31lo, bo);
       if (j == 0) {
@@ -436,49 +472,19 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t (&s
         Blo |= ((bo >> 15) & 1u) << (j - 1);
         Bhi |= (bo >> 31) << (j - 1);
       }
-      sp[j] = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
+      T[j] = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
     }
-    const uint64_t Bp = (uint64_t)Blo | ((uint64_t)Bhi << 32);
-    transpose32(sp);
-    emit_planes<uint64_t>(bw, 16, 63, 6, 4, [&](int i) -> uint64_t {
-      if (i == 16) return Bp;
-      return (uint64_t)(sp[i & 15] >> 1) | ((uint64_t)sp[16 + (i & 15)] << 31);
-    });
-    return;
+    topv = (uint64_t)Blo | ((uint64_t)Bhi << 32);
+    top = 16;
+    W = 63;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) T[j] = sp[j] ^ ((sp[j] >> 1) & 0x7FFF7FFFu);
   }
-  int W = 64, p = 6;
-  if (tag == kTagZBX) {
-    bw.put(mlo, 32);
-    bw.put(mhi, 32);
-    uint32_t cnt = 0;
+  transpose32(T);
 #pragma unroll
-    for (int half = 0; half < 2; ++half)
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        uint32_t v = half ? (sp[j] >> 16) : (sp[j] & 0xFFFFu);
-        if (v) {
-          sts16(scratch_addr(row, cnt >> 1, lane) + ((cnt & 1u) << 1), v);
-          ++cnt;
-        }
-      }
-    if (cnt == 0) return;
-    uint32_t rw[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) rw[r] = lds32(scratch_addr(row, r, lane));
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      uint32_t keep = (((uint32_t)j < cnt) ? 0x0000FFFFu : 0u) | (((uint32_t)j + 32 < cnt) ? 0xFFFF0000u : 0u);
-      sp[j] = split_word(rw, j) & keep;
-    }
-    W = (int)cnt;
-    p = ceil_log2_int(W);
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) sp[j] ^= (sp[j] >> 1) & 0x7FFF7FFFu;
-  transpose32(sp);
-  emit_planes<uint64_t>(bw, 15, W, p, 4, [&](int i) -> uint64_t {
-    return (uint64_t)sp[i & 15] | ((uint64_t)sp[16 + (i & 15)] << 32);
-  });
+  for (int i = 0; i < 32; ++i) sts32(plane_row(rowbase, lane, i), T[i]);
+  emit_plane_codes<true>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv);
 }
 
 // --------------------------------------------------------------- look-back
@@ -692,11 +698,11 @@ __global__ void __launch_bounds__(kEncWarps * 32, 2)
         BitWriter bw;
         bw.init(outbuf, off, kOutWords);
         bw.put(tag, 3);
-        const uint32_t row = smem_u32(st + lane * 128u);
+        const uint32_t rowbase = smem_u32(st) + lane * 128u;
         if (W16)
-          emit16(bw, tag, s, row, lane);
+          emit16(bw, tag, s, z.m0, z.m1, rowbase, lane);
         else
-          emit32(bw, tag, s, row, lane);
+          emit32(bw, tag, s, z.m0, rowbase, lane);
         bw.flush();
       }
     } else {
