@@ -105,6 +105,39 @@ pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width,
                         void *d_out, size_t nbytes, int *d_status,
                         pz_stream_t stream);
 
+/* Largest input pz_compress_noalloc accepts: 256 MiB (65,536 chunks). */
+#define PZ_NOALLOC_MAX_BYTES ((size_t)256 << 20)
+
+/* pz_compress without a scratch area in the caller's buffer. The paper has
+ * no counterpart: this entry point exists for callers that cannot allocate
+ * device memory when they compress. The typical one is a swap runtime that
+ * compresses activations precisely because device memory has run out: it
+ * cannot enlarge its output buffer by the scratch tail that pz_compress
+ * needs, and a code path that runs out of memory must not ask for more.
+ *
+ * It computes exactly what pz_compress computes (same kernel, same stream,
+ * same *d_total_bytes) but keeps the encoder's scratch (one 8-byte look-back
+ * word per chunk and a ticket counter) in a file-scope device array of the
+ * library, sized for PZ_NOALLOC_MAX_BYTES of input (about 512 KB); every GPU
+ * that loads the library holds that array until the process exits.
+ *   Arguments as for pz_compress, except:
+ *   out_capacity  must be >= 2*C + nbytes (the stream alone; C =
+ *                 ceil(nbytes / 4096)), else PZ_ERR_CAPACITY.
+ *   nbytes        must be <= PZ_NOALLOC_MAX_BYTES, else PZ_ERR_CAPACITY
+ *                 (nothing is enqueued).
+ * The call allocates nothing (no cudaMalloc, no allocating library call);
+ * it clears the scratch it needs with cudaMemsetAsync on `stream`.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. All calls in the process share the one array
+ * per device, which keeps the last call's contents: calls that may overlap
+ * on the GPU (different streams, or concurrent host threads) race on it and
+ * must be serialized by the caller. */
+pz_status pz_compress_noalloc(const void *d_in, size_t nbytes, int elem_width,
+                              void *d_out, size_t out_capacity,
+                              unsigned long long *d_total_bytes,
+                              pz_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     decompress_tensor,
     load,
     pz_compress,
+    pz_compress_noalloc,
     pz_decompress,
     pz_max_compressed_bytes,
 )

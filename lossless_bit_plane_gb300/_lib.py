@@ -17,7 +17,8 @@ LIB_PATH = Path(__file__).resolve().parent / "libplanezip.so"
 PZ_OK, PZ_ERR_ARG, PZ_ERR_CAPACITY, PZ_ERR_CORRUPT, PZ_ERR_CUDA, PZ_ERR_TIMEOUT = range(6)
 STATUS_NAMES = {0: "PZ_OK", 1: "PZ_ERR_ARG", 2: "PZ_ERR_CAPACITY", 3: "PZ_ERR_CORRUPT",
                 4: "PZ_ERR_CUDA", 5: "PZ_ERR_TIMEOUT"}
-EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress")
+EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress", "pz_compress_noalloc")
+NOALLOC_MAX_BYTES = 256 << 20  # PZ_NOALLOC_MAX_BYTES
 
 _lib = None
 
@@ -42,6 +43,8 @@ def load() -> ctypes.CDLL:
         L.pz_compress.restype = ctypes.c_int
         L.pz_decompress.argtypes = [vp, sz, ctypes.c_int, vp, sz, vp, vp]
         L.pz_decompress.restype = ctypes.c_int
+        L.pz_compress_noalloc.argtypes = [vp, sz, ctypes.c_int, vp, sz, vp, vp]
+        L.pz_compress_noalloc.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -61,6 +64,14 @@ def pz_decompress(d_in: int, comp_bytes: int, elem_width: int, d_out: int, nbyte
                   d_status: int, stream: int = 0) -> int:
     return int(load().pz_decompress(d_in or None, comp_bytes, elem_width, d_out or None, nbytes,
                                     d_status or None, stream or None))
+
+
+def pz_compress_noalloc(d_in: int, nbytes: int, elem_width: int, d_out: int, out_capacity: int,
+                        d_total_bytes: int, stream: int = 0) -> int:
+    """Raw C-ABI call of the allocation-free compress (scratch in a static
+    device array; out_capacity only needs 2*C + nbytes); returns the status."""
+    return int(load().pz_compress_noalloc(d_in or None, nbytes, elem_width, d_out or None, out_capacity,
+                                          d_total_bytes or None, stream or None))
 
 
 # ---------------------------------------------------------------- torch glue

@@ -160,3 +160,93 @@ pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, voi
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free compress: the same encoder launch as pz_compress, with the
+// look-back words and ticket counter in a file-scope device array instead of
+// the tail of the caller's output buffer. For callers that cannot allocate
+// when they compress (a swap runtime evicting activations because device
+// memory is full cannot grow its buffers); the declaration in planezip.h
+// states the limits and the sharing rules.
+namespace {
+
+constexpr size_t kNoAllocMaxChunks = PZ_NOALLOC_MAX_BYTES / kChunk;
+constexpr size_t kNoAllocScratchWords = kNoAllocMaxChunks + 8;  // status words + ticket
+static __device__ __align__(256) unsigned long long g_noalloc_scratch[kNoAllocScratchWords];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+cudaError_t noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" pz_status pz_compress_noalloc(const void *d_in, size_t nbytes, int elem_width, void *d_out,
+                                         size_t out_capacity, unsigned long long *d_total_bytes,
+                                         pz_stream_t stream) {
+  if (elem_width <= 0 || !d_total_bytes) return PZ_ERR_ARG;
+  const size_t C = num_chunks(nbytes);
+  if (nbytes && (!d_in || !d_out)) return PZ_ERR_ARG;
+  if (nbytes && (!aligned16(d_in) || !aligned16(d_out))) return PZ_ERR_ARG;
+  if (nbytes > PZ_NOALLOC_MAX_BYTES) return PZ_ERR_CAPACITY;
+  if (out_capacity < 2 * C + nbytes) return PZ_ERR_CAPACITY;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
+  if (nbytes == 0) return PZ_OK;
+
+  DeviceInfo info;
+  if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
+  void *scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return PZ_ERR_CUDA;
+  // the previous call's look-back words and ticket must not leak into this one
+  if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
+
+  pz::EncodeArgs a;
+  a.in = static_cast<const uint8_t *>(d_in);
+  a.out = static_cast<uint8_t *>(d_out);
+  a.status = static_cast<unsigned long long *>(scratch);
+  a.ticket = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(scratch) + 8 * C);
+  a.total = d_total_bytes;
+  a.nbytes = nbytes;
+  a.num_chunks = (uint32_t)C;
+  a.tma_rows = nbytes / 128;
+
+  alignas(64) CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  if (a.tma_rows > 0) {
+    cuuint64_t dims[2] = {32, (cuuint64_t)a.tma_rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(d_in), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return PZ_ERR_CUDA;
+  }
+  const bool w16 = (elem_width == 2);
+  const int warps = pz::encode_warps();
+  size_t grid = (size_t)info.enc_ctas_per_sm[w16 ? 1 : 0] * info.sms;
+  const size_t need = (C + warps - 1) / warps;
+  if (grid > need) grid = need;
+  void *args[2] = {&tmap, &a};
+  if (cudaLaunchKernel(pz::encode_kernel_ptr(w16), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
+                       pz::encode_smem_bytes(), s) != cudaSuccess)
+    return PZ_ERR_CUDA;
+  return PZ_OK;
+}
