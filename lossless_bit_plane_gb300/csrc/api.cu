@@ -150,11 +150,15 @@ pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, voi
   a.nbytes = nbytes;
   a.status = d_status;
   a.num_chunks = (uint32_t)C;
-  const size_t per = (size_t)pz::decode_chunks_per_cta();
-  const size_t grid = (C + per - 1) / per;
+  const bool w16 = (elem_width == 2);
   void *args[1] = {&a};
-  if (cudaLaunchKernel(pz::decode_kernel_ptr(elem_width == 2), dim3((unsigned)grid), dim3(pz::decode_threads()),
-                       args, 0, s) != cudaSuccess)
+  const size_t wt = (size_t)pz::walk_threads();
+  if (cudaLaunchKernel(pz::walk_kernel_ptr(w16), dim3((unsigned)((C + wt - 1) / wt)), dim3((unsigned)wt), args, 0,
+                       s) != cudaSuccess)
+    return PZ_ERR_CUDA;
+  const size_t per = (size_t)pz::decode_chunks_per_cta();
+  if (cudaLaunchKernel(pz::decode_kernel_ptr(w16), dim3((unsigned)((C + per - 1) / per)),
+                       dim3(pz::decode_threads()), args, 0, s) != cudaSuccess)
     return PZ_ERR_CUDA;
   return PZ_OK;
 }

@@ -36,8 +36,7 @@
 
 namespace pz {
 
-constexpr int kDecWarps = 4;
-constexpr int kDecChunksPerCta = 32 * kDecWarps;
+constexpr int kDecWarps = 8;
 
 // LSB-first reader over the stream's 32-bit words with one word prefetched.
 struct BitReader {
@@ -286,130 +285,357 @@ __device__ __forceinline__ bool decode_block(BitReader &br, uint32_t (&o)[32], u
   return true;
 }
 
-// ---------------------------------------------------------------- kernel
+// ------------------------------------------------------ block boundaries
+// The format stores no per-block offsets, so a chunk's block starts come from
+// a walk that only measures code lengths (tags, masks, plane-code prefixes).
 
-template <bool W16>
-__global__ void __launch_bounds__(kDecWarps * 32)
-    decode_kernel(DecodeArgs p) {
-  __shared__ unsigned long long red[kDecWarps];
-  __shared__ uint32_t wsum[kDecWarps];
-  __shared__ __align__(16) uint32_t scratch[kDecWarps][32 * 32];
-  const uint32_t lane = lane_id();
-  const uint32_t warp = threadIdx.x >> 5;
-  const uint32_t C = p.num_chunks;
-  const uint32_t first = blockIdx.x * kDecChunksPerCta;
-  const uint16_t *hdr = reinterpret_cast<const uint16_t *>(p.in);
+// 32 stream bits starting at an absolute bit position (reads clamped to the
+// input, so a malformed length never reads outside it).
+struct Window {
+  const uint32_t *w;
+  uint64_t nw;
+  __device__ __forceinline__ uint32_t ld(uint64_t i) const { return i < nw ? __ldg(w + i) : 0u; }
+  __device__ __forceinline__ uint32_t peek32(uint64_t pos) const {
+    const uint64_t wi = pos >> 5;
+    return __funnelshift_r(ld(wi), ld(wi + 1), (uint32_t)(pos & 31));
+  }
+};
 
-  // sum of all chunk sizes before this CTA's first chunk
-  unsigned long long part = 0;
-  {
-    const uint4 *h4 = reinterpret_cast<const uint4 *>(p.in);  // first is a multiple of 8
-    for (uint32_t i = threadIdx.x; i < first / 8; i += blockDim.x) {
-      uint4 v = __ldg(h4 + i);
-      part += (v.x & 0xFFFFu) + (v.x >> 16) + (v.y & 0xFFFFu) + (v.y >> 16) + (v.z & 0xFFFFu) +
-              (v.z >> 16) + (v.w & 0xFFFFu) + (v.w >> 16);
+// Reader over one chunk's bits at chunk-relative positions.
+struct WindowReader {  // straight from global memory (clamped to the input)
+  Window win;
+  uint64_t base;
+  __device__ __forceinline__ uint32_t peek(uint32_t pos) const { return win.peek32(base + pos); }
+};
+
+// Lane-private 512-byte ring in shared memory, filled ahead of the read
+// position with 16-byte cp.async copies (one commit group per copy), so a
+// lane streams its chunk without scattered global loads.
+constexpr uint32_t kRingUnits = 32;  // 16-byte units per ring
+constexpr uint32_t kRingAhead = 24;  // units kept in flight past the read unit
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_ahead() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kRingAhead) : "memory");
+}
+
+struct RingReader {
+  uint32_t ring;       // shared address of the lane's ring
+  const uint8_t *g0;   // 16-byte aligned global address of unit 0
+  uint32_t nunits;     // units that hold chunk bytes
+  uint32_t fetched;    // units issued so far
+  uint32_t ready;      // units known to be resident
+  uint32_t bit0;       // bit of unit 0 where the chunk starts
+
+  __device__ __forceinline__ void init(uint32_t ring_addr, const uint8_t *in, uint64_t off, uint32_t L) {
+    const uint64_t a0 = off & ~15ull;
+    ring = ring_addr;
+    g0 = in + a0;
+    bit0 = (uint32_t)(off - a0) * 8u;
+    nunits = (uint32_t)((off + L + 15 - a0) >> 4);
+    fetched = 0;
+    ready = 0;
+  }
+  __device__ __forceinline__ uint32_t peek(uint32_t pos) {
+    const uint32_t q = bit0 + pos;
+    const uint32_t need = ((q + 63) >> 7) + 1;  // units under a 64-bit window at q
+    if (need > ready) {
+      const uint32_t lim = min(need + kRingAhead, nunits);
+      while (fetched < lim) {
+        cp_async16(ring + (fetched % kRingUnits) * 16u, g0 + 16ull * fetched);
+        ++fetched;
+      }
+      if (fetched == nunits) {
+        cp_async_wait_all();
+        ready = 0xFFFFFFFFu;
+      } else {
+        cp_async_wait_ahead();
+        ready = fetched - kRingAhead;
+      }
+    }
+    const uint32_t w = q >> 5;
+    uint32_t lo, hi;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(lo) : "r"(ring + (w % (kRingUnits * 4)) * 4u) : "memory");
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hi) : "r"(ring + ((w + 1) % (kRingUnits * 4)) * 4u) : "memory");
+    return __funnelshift_r(lo, hi, q & 31u);
+  }
+};
+
+// Advance pos over the plane codes of planes top..0 of width W.
+template <typename Reader>
+__device__ __forceinline__ bool walk_planes(Reader &rd, uint32_t &pos, int top, int W, int K) {
+  const int p = ceil_log2_int(W);
+  int i = top;
+#pragma unroll 1
+  while (i >= 0) {
+    const uint32_t v = rd.peek(pos);
+    if (v & 1u) {  // verbatim
+      pos += 1 + W;
+      i -= 1;
+    } else if ((v & 3u) == 2u) {  // zero run
+      const int L = 2 + (int)((v >> 2) & ((1u << K) - 1));
+      if (L > i + 1) return false;
+      pos += 2 + K;
+      i -= L;
+    } else if ((v & 7u) == 4u) {  // single zero plane
+      pos += 3;
+      i -= 1;
+    } else {  // 5-bit codes, position field for 0 0 0 1 x
+      const uint32_t code = v & 31u;
+      if (code == 16u && i == top) return false;
+      pos += 5 + ((code & 8u) ? p : 0);
+      i -= 1;
     }
   }
-  part = warp_sum_u64(part);
-  // this CTA's own headers
-  const uint32_t c = first + warp * 32 + lane;
+  return true;
+}
+
+// Record each block's start bit (relative to the chunk) and check that the
+// chunk is exactly ceil(bits/8) bytes with zero padding.
+template <bool W16, typename Reader>
+__device__ __forceinline__ bool walk_chunk(Reader &rd, uint32_t L, uint32_t nblk, uint16_t *starts) {
+  constexpr int w = W16 ? 16 : 32;
+  constexpr int N = W16 ? 64 : 32;
+  constexpr int K = W16 ? 4 : 5;
+  const uint32_t cap = 8u * L;
+  uint32_t pos = 0;
+#pragma unroll 1
+  for (uint32_t b = 0; b < nblk; ++b) {
+    starts[b] = (uint16_t)pos;
+    const uint32_t tag = rd.peek(pos) & 7u;
+    pos += 3;
+    if (tag > kTagRAW) return false;
+    if (tag == kTagRAW) {
+      pos += 1024;
+    } else if (tag == kTagZVC || tag == kTagZBX) {
+      uint32_t n = __popc(rd.peek(pos));
+      pos += 32;
+      if (W16) {
+        n += __popc(rd.peek(pos));
+        pos += 32;
+      }
+      if (tag == kTagZVC)
+        pos += n * w;
+      else if (n && !walk_planes(rd, pos, w - 1, (int)n, K))
+        return false;
+    } else {
+      int top = w - 1, W = N;
+      if (tag == kTagDBX) {
+        pos += w;
+        top = w;
+        W = N - 1;
+      }
+      if (!walk_planes(rd, pos, top, W, K)) return false;
+    }
+    if (pos > cap) return false;
+  }
+  if (cap - pos >= 8) return false;
+  if (cap > pos && (rd.peek(pos) & ((1u << (cap - pos)) - 1u))) return false;
+  return true;
+}
+
+// ---------------------------------------------------------------- kernels
+//
+// Two launches. The walk kernel runs one thread per chunk: it finds the
+// chunk's payload offset (sum of all earlier sizes) and, for a coded chunk,
+// every block's start bit, and leaves them in the first bytes of that
+// chunk's own output region: the offset (8 bytes) then the start bits of
+// blocks 1..n-1 (2 bytes each). The decode kernel runs one warp per chunk,
+// lane = block: each lane reads its start, the warp synchronises, and only
+// then are those bytes overwritten with decoded data. A final chunk too
+// short to hold that record (under 72 bytes) is located and walked by its
+// decode warp instead.
+
+constexpr int kWalkThreads = 64;
+constexpr int kRecordBytes = 72;  // 8-byte offset + 31 x 2-byte start bits + padding
+
+// Sum of the 16-bit sizes of chunks [0, first) by all threads of the block;
+// first must be a multiple of 8.
+__device__ __forceinline__ unsigned long long sum_sizes_before(const uint8_t *in, uint32_t first) {
+  unsigned long long part = 0;
+  const uint4 *h4 = reinterpret_cast<const uint4 *>(in);
+  for (uint32_t i = threadIdx.x; i < first / 8; i += blockDim.x) {
+    const uint4 v = __ldg(h4 + i);
+    part += (v.x & 0xFFFFu) + (v.x >> 16) + (v.y & 0xFFFFu) + (v.y >> 16) + (v.z & 0xFFFFu) + (v.z >> 16) +
+            (v.w & 0xFFFFu) + (v.w >> 16);
+  }
+  return part;
+}
+
+template <bool W16>
+__global__ void __launch_bounds__(kWalkThreads)
+    walk_kernel(DecodeArgs p) {
+  __shared__ __align__(16) uint8_t rings[kWalkThreads][kRingUnits * 16];
+  __shared__ unsigned long long red[kWalkThreads / 32];
+  __shared__ uint32_t wsum[kWalkThreads / 32];
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t C = p.num_chunks;
+  const uint32_t first = blockIdx.x * kWalkThreads;
+  unsigned long long part = warp_sum_u64(sum_sizes_before(p.in, first));
+  const uint32_t c = first + threadIdx.x;
   const bool valid = c < C;
-  const uint32_t L = valid ? __ldg(hdr + c) : 0u;
+  const uint32_t L = valid ? __ldg(reinterpret_cast<const uint16_t *>(p.in) + c) : 0u;
   uint32_t incl = L;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= (uint32_t)o) incl += v;
   }
-  if (lane == 31) wsum[warp] = incl;
   if (lane == 0) red[warp] = part;
+  if (lane == 31) wsum[warp] = incl;
   __syncthreads();
+  if (!valid) return;
   unsigned long long base = 0;
-  for (int w = 0; w < kDecWarps; ++w) base += red[w];
+  for (int w = 0; w < kWalkThreads / 32; ++w) base += red[w];
   for (uint32_t w = 0; w < warp; ++w) base += wsum[w];
-  const uint64_t off = base + (incl - L);  // payload offset after the header table
+  const uint64_t off = 2ull * C + base + (incl - L);
+  const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
+  if (L == 0 || L > raw_len || off + L > p.comp_bytes) {
+    atomicMax(p.status, kErrCorrupt);
+    return;
+  }
+  if (raw_len < (uint32_t)kRecordBytes) return;  // the decode warp handles it
+  uint8_t *rec = p.out + (uint64_t)c * 4096u;
+  *reinterpret_cast<unsigned long long *>(rec) = off;
+  if (L == raw_len) return;  // raw chunk: the offset is all the decoder needs
+  uint16_t starts[32];
+  RingReader rd;
+  rd.init(smem_u32(rings[threadIdx.x]), p.in, off, L);
+  const uint32_t nblk = (raw_len + 127u) >> 7;
+  const bool ok = walk_chunk<W16>(rd, L, nblk, starts);
+  cp_async_wait_all();  // no copy may be in flight when the thread exits
+  if (!ok) {
+    atomicMax(p.status, kErrCorrupt);
+    return;
+  }
+  uint16_t *rs = reinterpret_cast<uint16_t *>(rec + 8);
+#pragma unroll 1
+  for (uint32_t b = 1; b < nblk; ++b) rs[b - 1] = starts[b];
+}
 
+// Byte offset of 16-byte unit u of row r in a 128-byte-swizzled 4 KB tile.
+__device__ __forceinline__ uint32_t tile_swz(uint32_t r, uint32_t u) { return r * 128u + ((u ^ (r & 7u)) << 4); }
+
+template <bool W16>
+__global__ void __launch_bounds__(kDecWarps * 32, 2)
+    decode_kernel(DecodeArgs p) {
+  __shared__ __align__(16) uint32_t tile[kDecWarps][32 * 32];  // per warp: 32 lane rows of 128 B
+  __shared__ uint16_t tail_starts[kDecWarps][32];
+  const uint32_t lane = lane_id();
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t C = p.num_chunks;
+  const uint32_t c = blockIdx.x * kDecWarps + warp;
+  if (c >= C) return;
+  const uint32_t L = __ldg(reinterpret_cast<const uint16_t *>(p.in) + c);
+  const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
   const uint64_t hdr_bytes = 2ull * C;
-  const uint64_t c0 = (uint64_t)c * 4096u;
-  const uint32_t raw_len = valid ? (uint32_t)umin64(4096u, p.nbytes - c0) : 0u;
-  bool bad = valid && (L == 0 || L > raw_len || hdr_bytes + off + L > p.comp_bytes);
-  if (bad) atomicMax(p.status, kErrCorrupt);
-  const bool is_raw = valid && !bad && L == raw_len;
-  const bool is_coded = valid && !bad && L < raw_len;
+  if (L == 0 || L > raw_len) return;  // reported by the walk kernel
+  uint8_t *dst = p.out + (uint64_t)c * 4096u;
+  const uint32_t nblk = (raw_len + 127u) >> 7;
+  const Window win{reinterpret_cast<const uint32_t *>(p.in), (p.comp_bytes + 3) / 4};
 
-  // raw chunks: the whole warp copies each one (unaligned source)
-  uint32_t rm = __ballot_sync(0xFFFFFFFFu, is_raw);
-  while (rm) {
-    const uint32_t src_lane = __ffs(rm) - 1;
-    rm &= rm - 1;
-    const uint64_t soff = __shfl_sync(0xFFFFFFFFu, hdr_bytes + off, src_lane);
-    const uint32_t rl = __shfl_sync(0xFFFFFFFFu, raw_len, src_lane);
-    const uint32_t cc = __shfl_sync(0xFFFFFFFFu, c, src_lane);
+  // payload offset and this lane's block start bit
+  uint64_t off;
+  uint32_t s0 = 0, s1 = 0;
+  bool ok = true;
+  if (raw_len >= (uint32_t)kRecordBytes) {
+    off = *reinterpret_cast<const unsigned long long *>(dst);
+    if (L < raw_len) {
+      const uint16_t *rs = reinterpret_cast<const uint16_t *>(dst + 8);
+      s0 = (lane >= 1 && lane < nblk) ? rs[lane - 1] : 0u;
+      s1 = (lane + 1 < nblk) ? rs[lane] : 0u;
+    }
+  } else {  // short final chunk: locate and walk it here
+    unsigned long long part = 0;
+    for (uint32_t i = lane; i < c; i += 32) part += __ldg(reinterpret_cast<const uint16_t *>(p.in) + i);
+    off = hdr_bytes + warp_sum_u64(part);
+    if (off + L > p.comp_bytes) return;  // reported by the walk kernel
+    if (L < raw_len) {
+      if (lane == 0) {
+        WindowReader rd{win, 8ull * off};
+        ok = walk_chunk<W16>(rd, L, nblk, tail_starts[warp]);
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        if (lane == 0) atomicMax(p.status, kErrCorrupt);
+        return;
+      }
+      __syncwarp();
+      s0 = (lane < nblk) ? tail_starts[warp][lane] : 0u;
+      s1 = (lane + 1 < nblk) ? tail_starts[warp][lane + 1] : 0u;
+    }
+  }
+  if (off + L > p.comp_bytes) return;  // reported by the walk kernel
+  __syncwarp();  // every lane has read the record before any output is written
+
+  if (L == raw_len) {  // raw chunk: the warp copies it (source at any byte offset)
     const uint32_t *w = reinterpret_cast<const uint32_t *>(p.in);
     const uint64_t nw = (p.comp_bytes + 3) / 4;
-    uint8_t *dst = p.out + (uint64_t)cc * 4096u;
-    const uint32_t sh = (uint32_t)(soff & 3) * 8;
-    for (uint32_t v = lane; v * 16 < rl; v += 32) {
-      const uint64_t wi = (soff + 16ull * v) >> 2;
+    const uint32_t sh = (uint32_t)(off & 3) * 8;
+    for (uint32_t v = lane; v * 16 < raw_len; v += 32) {
+      const uint64_t wi = (off + 16ull * v) >> 2;
       uint32_t w5[5];
 #pragma unroll
       for (int k = 0; k < 5; ++k) w5[k] = (wi + k < nw) ? __ldg(w + wi + k) : 0u;
       uint32_t o[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(w5[k], w5[k + 1], sh);
-      if (v * 16 + 16 <= rl) {
+      if (v * 16 + 16 <= raw_len) {
         *reinterpret_cast<uint4 *>(dst + 16ull * v) = make_uint4(o[0], o[1], o[2], o[3]);
       } else {
-        for (uint32_t b = 0; v * 16 + b < rl; ++b) dst[16ull * v + b] = (uint8_t)(o[b >> 2] >> ((b & 3) * 8));
+        for (uint32_t b = 0; v * 16 + b < raw_len; ++b) dst[16ull * v + b] = (uint8_t)(o[b >> 2] >> ((b & 3) * 8));
       }
     }
+    return;
   }
 
-  // coded chunks: each lane walks its own chunk
-  if (is_coded) {
+  uint32_t *tw = tile[warp];
+  const uint32_t row = smem_u32(tw) + lane * 128u;
+  if (lane < nblk) {
     BitReader br;
-    br.init(reinterpret_cast<const uint32_t *>(p.in), (p.comp_bytes + 3) / 4, 8ull * (hdr_bytes + off));
-    const uint32_t nblk = (raw_len + 127u) >> 7;
-    const uint32_t row = smem_u32(&scratch[warp][lane * 32]);
-    uint8_t *dst = p.out + c0;
-    bool ok = true;
-    for (uint32_t b = 0; b < nblk && ok; ++b) {
-      uint32_t s[32];
-      ok = decode_block<W16>(br, s, row, lane);
-      if (br.consumed > 8ull * L) ok = false;
-      if (!ok) break;
-      uint8_t *bd = dst + 128u * b;
-      const uint32_t take = min(128u, raw_len - 128u * b);
-      if (take == 128u) {
+    br.init(reinterpret_cast<const uint32_t *>(p.in), (p.comp_bytes + 3) / 4, 8ull * off + s0);
+    uint32_t o[32];
+    ok = decode_block<W16>(br, o, row, lane);
+    if (lane + 1 < nblk && br.consumed != s1 - s0) ok = false;
+    if (lane + 1 == nblk && s0 + br.consumed > 8u * L) ok = false;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          reinterpret_cast<uint4 *>(bd)[u] = make_uint4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
-      } else {
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(tw) + tile_swz(lane, u)) =
+          make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+  }
+  if (!ok) atomicMax(p.status, kErrCorrupt);
+  __syncwarp();
+  // coalesced write-out of the chunk
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if ((uint32_t)(4 * k + e) < take) bd[4 * k + e] = (uint8_t)(s[k] >> (8 * e));
-      }
+  for (uint32_t i = 0; i < 8; ++i) {
+    const uint32_t v = lane + 32u * i;
+    if (16u * v >= raw_len) break;
+    const uint4 q = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(tw) + tile_swz(v >> 3, v & 7));
+    if (16u * v + 16u <= raw_len) {
+      *reinterpret_cast<uint4 *>(dst + 16u * v) = q;
+    } else {
+      const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+      for (uint32_t b = 0; 16u * v + b < raw_len; ++b) dst[16u * v + b] = (uint8_t)(qq[b >> 2] >> ((b & 3) * 8));
     }
-    if (ok) {
-      // exactly ceil(bits/8) bytes, zero padding
-      const uint64_t cap = 8ull * L;
-      if (cap - br.consumed >= 8) ok = false;
-      else {
-        const uint32_t pad = (uint32_t)(cap - br.consumed);
-        if (pad && br.get(pad) != 0) ok = false;
-      }
-    }
-    if (!ok) atomicMax(p.status, kErrCorrupt);
   }
 }
 
+template __global__ void walk_kernel<false>(DecodeArgs);
+template __global__ void walk_kernel<true>(DecodeArgs);
 template __global__ void decode_kernel<false>(DecodeArgs);
 template __global__ void decode_kernel<true>(DecodeArgs);
 
+int walk_threads() { return kWalkThreads; }
 int decode_threads() { return kDecWarps * 32; }
-int decode_chunks_per_cta() { return kDecChunksPerCta; }
+int decode_chunks_per_cta() { return kDecWarps; }
+const void *walk_kernel_ptr(bool w16) {
+  return w16 ? reinterpret_cast<const void *>(&walk_kernel<true>)
+             : reinterpret_cast<const void *>(&walk_kernel<false>);
+}
 const void *decode_kernel_ptr(bool w16) {
   return w16 ? reinterpret_cast<const void *>(&decode_kernel<true>)
              : reinterpret_cast<const void *>(&decode_kernel<false>);

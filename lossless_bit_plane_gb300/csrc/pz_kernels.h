@@ -33,6 +33,8 @@ int encode_threads();
 int encode_warps();
 const void *encode_kernel_ptr(bool w16);
 
+int walk_threads();
+const void *walk_kernel_ptr(bool w16);
 int decode_threads();
 int decode_chunks_per_cta();
 const void *decode_kernel_ptr(bool w16);
