@@ -328,8 +328,8 @@ struct RingReader {
   const uint8_t *g0;   // 16-byte aligned global address of unit 0
   uint32_t nunits;     // units that hold chunk bytes
   uint32_t fetched;    // units issued so far
-  uint32_t ready;      // units known to be resident
   uint32_t bit0;       // bit of unit 0 where the chunk starts
+  uint32_t limit;      // a peek at any q = bit0 + pos below this is resident
 
   __device__ __forceinline__ void init(uint32_t ring_addr, const uint8_t *in, uint64_t off, uint32_t L) {
     const uint64_t a0 = off & ~15ull;
@@ -338,60 +338,85 @@ struct RingReader {
     bit0 = (uint32_t)(off - a0) * 8u;
     nunits = (uint32_t)((off + L + 15 - a0) >> 4);
     fetched = 0;
-    ready = 0;
+    limit = 0;
   }
-  __device__ __forceinline__ uint32_t peek(uint32_t pos) {
-    const uint32_t q = bit0 + pos;
+  __device__ __forceinline__ void refill(uint32_t q) {
     const uint32_t need = ((q + 63) >> 7) + 1;  // units under a 64-bit window at q
-    if (need > ready) {
-      const uint32_t lim = min(need + kRingAhead, nunits);
-      while (fetched < lim) {
-        cp_async16(ring + (fetched % kRingUnits) * 16u, g0 + 16ull * fetched);
-        ++fetched;
-      }
-      if (fetched == nunits) {
-        cp_async_wait_all();
-        ready = 0xFFFFFFFFu;
-      } else {
-        cp_async_wait_ahead();
-        ready = fetched - kRingAhead;
-      }
+    const uint32_t lim = min(need + kRingAhead, nunits);
+    while (fetched < lim) {
+      cp_async16(ring + (fetched % kRingUnits) * 16u, g0 + 16ull * fetched);
+      ++fetched;
     }
+    if (fetched == nunits) {
+      cp_async_wait_all();
+      limit = 0xFFFFFFFFu;
+    } else {
+      cp_async_wait_ahead();
+      limit = (fetched - kRingAhead) * 128u - 63u;  // q + 63 < resident units * 128
+    }
+  }
+  // 32 bits at chunk bit pos; the caller has ensured residency
+  __device__ __forceinline__ uint32_t peek_resident(uint32_t pos) const {
+    const uint32_t q = bit0 + pos;
     const uint32_t w = q >> 5;
     uint32_t lo, hi;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(lo) : "r"(ring + (w % (kRingUnits * 4)) * 4u) : "memory");
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hi) : "r"(ring + ((w + 1) % (kRingUnits * 4)) * 4u) : "memory");
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(lo) : "r"(ring + ((w & (kRingUnits * 4 - 1)) << 2)) : "memory");
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hi) : "r"(ring + (((w + 1) & (kRingUnits * 4 - 1)) << 2)) : "memory");
     return __funnelshift_r(lo, hi, q & 31u);
+  }
+  // make every peek at or below pos resident
+  __device__ __forceinline__ void ensure(uint32_t pos) {
+    const uint32_t q = bit0 + pos;
+    if (q >= limit) refill(q);
+  }
+  __device__ __forceinline__ uint32_t peek(uint32_t pos) {
+    ensure(pos);
+    return peek_resident(pos);
   }
 };
 
-// Advance pos over the plane codes of planes top..0 of width W.
+struct WindowPeeker {  // adapts WindowReader to the ensure / peek_resident interface
+  WindowReader r;
+  __device__ __forceinline__ void ensure(uint32_t) const {}
+  __device__ __forceinline__ uint32_t peek_resident(uint32_t pos) const { return r.peek(pos); }
+  __device__ __forceinline__ uint32_t peek(uint32_t pos) const { return r.peek(pos); }
+};
+
+// Advance pos over the plane codes of planes top..0 of width W. Each step
+// tests the flag bit of the next four codes under the assumption that they
+// are verbatim (a verbatim code is 1 + W bits): a run of m leading verbatim
+// codes advances m planes at once; otherwise the code at pos is classified
+// by its leading zero bits (stream order, capped at 4): 01 run (2+K bits,
+// 2+field planes), 001 single zero (3), 0001x position code (5+p), 0000x
+// all-ones / pre-XOR-zero (5).
 template <typename Reader>
 __device__ __forceinline__ bool walk_planes(Reader &rd, uint32_t &pos, int top, int W, int K) {
-  const int p = ceil_log2_int(W);
+  const uint32_t p = (uint32_t)ceil_log2_int(W);
+  const uint32_t S = 1u + (uint32_t)W;
+  const uint32_t kmask = (1u << K) - 1u;
   int i = top;
+  bool ok = true;
 #pragma unroll 1
   while (i >= 0) {
-    const uint32_t v = rd.peek(pos);
-    if (v & 1u) {  // verbatim
-      pos += 1 + W;
-      i -= 1;
-    } else if ((v & 3u) == 2u) {  // zero run
-      const int L = 2 + (int)((v >> 2) & ((1u << K) - 1));
-      if (L > i + 1) return false;
-      pos += 2 + K;
-      i -= L;
-    } else if ((v & 7u) == 4u) {  // single zero plane
-      pos += 3;
-      i -= 1;
-    } else {  // 5-bit codes, position field for 0 0 0 1 x
-      const uint32_t code = v & 31u;
-      if (code == 16u && i == top) return false;
-      pos += 5 + ((code & 8u) ? p : 0);
-      i -= 1;
+    rd.ensure(pos + 3u * S);
+    const uint32_t v0 = rd.peek_resident(pos);
+    const uint32_t f = (v0 & 1u) | ((rd.peek_resident(pos + S) & 1u) << 1) |
+                       ((rd.peek_resident(pos + 2u * S) & 1u) << 2) | ((rd.peek_resident(pos + 3u * S) & 1u) << 3);
+    int m = __ffs(~f) - 1;  // leading verbatim codes, 0..4
+    if (m > i + 1) m = i + 1;
+    if (m > 0) {
+      pos += (uint32_t)m * S;
+      i -= m;
+      continue;
     }
+    const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4
+    const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + p : 5u;
+    const int run = (tz == 1u) ? 2 + (int)((v0 >> 2) & kmask) : 1;
+    ok = ok && !(run > i + 1) && !(tz == 4u && (v0 & 16u) && i == top);
+    pos += len;
+    i -= run;
   }
-  return true;
+  return ok;
 }
 
 // Record each block's start bit (relative to the chunk) and check that the
@@ -556,7 +581,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
     if (off + L > p.comp_bytes) return;  // reported by the walk kernel
     if (L < raw_len) {
       if (lane == 0) {
-        WindowReader rd{win, 8ull * off};
+        WindowPeeker rd{WindowReader{win, 8ull * off}};
         ok = walk_chunk<W16>(rd, L, nblk, tail_starts[warp]);
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
