@@ -37,58 +37,7 @@
 namespace pz {
 
 constexpr int kDecWarps = 8;
-
-// LSB-first reader over the stream's 32-bit words with one word prefetched.
-struct BitReader {
-  const uint32_t *words;
-  uint64_t nwords;  // words that hold at least one stream byte
-  uint64_t wpos;    // index of the word held in nxt
-  uint64_t buf;
-  uint32_t nbuf;
-  uint32_t nxt;
-  uint64_t consumed;
-
-  __device__ __forceinline__ uint32_t load(uint64_t i) const { return i < nwords ? __ldg(words + i) : 0u; }
-  __device__ __forceinline__ void init(const uint32_t *w, uint64_t nw, uint64_t bitpos) {
-    words = w;
-    nwords = nw;
-    uint64_t wi = bitpos >> 5;
-    uint32_t sh = (uint32_t)(bitpos & 31);
-    buf = (uint64_t)load(wi) >> sh;
-    nbuf = 32 - sh;
-    wpos = wi + 1;
-    nxt = load(wpos);
-    consumed = 0;
-  }
-  __device__ __forceinline__ void ensure(uint32_t n) {  // n <= 32
-    if (nbuf < n) {
-      buf |= (uint64_t)nxt << nbuf;
-      nbuf += 32;
-      nxt = load(++wpos);
-    }
-  }
-  __device__ __forceinline__ uint32_t peek(uint32_t n) const {  // after ensure(n), n <= 32
-    return (uint32_t)buf & (uint32_t)((1ull << n) - 1);
-  }
-  __device__ __forceinline__ void skip(uint32_t n) {
-    buf >>= n;
-    nbuf -= n;
-    consumed += n;
-  }
-  __device__ __forceinline__ uint32_t get(uint32_t n) {  // n <= 32
-    ensure(n);
-    uint32_t v = peek(n);
-    skip(n);
-    return v;
-  }
-  __device__ __forceinline__ uint64_t get64(uint32_t n) {  // n <= 64
-    if (n > 32) {
-      uint64_t lo = get(32);
-      return lo | ((uint64_t)get(n - 32) << 32);
-    }
-    return get(n);
-  }
-};
+constexpr uint32_t kStageWords = (4096 + 16) / 4 + 4;  // 257 16-byte units + slack for 64-bit peeks
 
 __device__ __forceinline__ uint32_t lds32d(uint32_t addr) {
   uint32_t v;
@@ -114,95 +63,67 @@ __device__ __forceinline__ uint32_t prow_half(uint32_t row, uint32_t lane, uint3
   return prow(row, lane, h >> 1) + ((h & 1u) << 1);
 }
 
-// Parse the P = top+1 plane codes of one block, top plane first, rebuilding
-// the pre-XOR planes P_i = X_i ^ P_{i+1}, and store them in the lane's row:
-// FP32 plane i < 32 in word i; BF16 plane i < 16 in words i (symbols 0..31)
-// and 16+i (symbols 32..63). For DBX the rows are pre-shifted so that row
-// bit j holds delta j (plane bit q is delta q+1); the top DBX plane (the
-// borrow plane) is not stored. Returns false on a malformed code.
-template <bool W16>
-__device__ __forceinline__ bool parse_plane_rows(BitReader &br, uint32_t row, uint32_t lane, int top, int W,
-                                                 int p, bool dbx) {
-  const int K = W16 ? 4 : 5;
-  const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
-  uint64_t Pup = 0;
-  int run = 0;
-#pragma unroll 1
-  for (int i = top; i >= 0; --i) {
-    uint64_t X = 0;
-    if (run > 0) {
-      --run;
-    } else {
-      br.ensure(16);
-      const uint32_t v = br.peek(16);
-      if (v & 1u) {  // 1 + plane
-        br.skip(1);
-        X = br.get64((uint32_t)W);
-      } else if ((v & 3u) == 2u) {  // 0 1 + (run - 2)
-        const int L = 2 + (int)((v >> 2) & ((1u << K) - 1));
-        br.skip(2 + K);
-        if (L > i + 1) return false;
-        run = L - 1;
-      } else if ((v & 7u) == 4u) {  // 0 0 1
-        br.skip(3);
-      } else {
-        const uint32_t code = v & 31u;
-        br.skip(5);
-        if (code == 0) {  // 0 0 0 0 0: all ones
-          X = full;
-        } else if (code == 16) {  // 0 0 0 0 1: pre-XOR plane zero
-          if (i == top) return false;
-          X = Pup;
-        } else {  // 0 0 0 1 0 / 0 0 0 1 1 + q
-          const int q = (int)br.get((uint32_t)p);
-          if (code == 8) {
-            if (q + 1 >= W) return false;
-            X = 3ull << q;
-          } else {
-            if (q >= W) return false;
-            X = 1ull << q;
-          }
-        }
-      }
-    }
-    const uint64_t Pi = (i == top) ? X : (X ^ Pup);
-    Pup = Pi;
-    if (W16) {
-      if (i < 16) {
-        sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
-        sts32d(prow(row, lane, (uint32_t)i + 16), dbx ? (uint32_t)(Pi >> 31) : (uint32_t)(Pi >> 32));
-      }
-    } else {
-      if (i < 32) sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
-    }
+// A chunk's payload staged in shared memory: word k holds stream bytes
+// [a0 + 4k, a0 + 4k + 4), where a0 is the payload's first byte rounded down
+// to 16; bit q counts from a0. The buffer has slack words past the data.
+struct StageBits {
+  uint32_t base;  // shared address of word 0
+  // word address of bit q, clamped so that a malformed stream cannot read
+  // outside the buffer (valid streams never reach the clamp)
+  __device__ __forceinline__ uint32_t addr(uint32_t q) const { return base + (min(q >> 5, kStageWords - 3u) << 2); }
+  __device__ __forceinline__ uint32_t peek32(uint32_t q) const {
+    const uint32_t a = addr(q);
+    return __funnelshift_r(lds32d(a), lds32d(a + 4), q & 31u);
   }
-  return true;
-}
+  // bits [q, q + 64) and bit q + 64
+  __device__ __forceinline__ uint64_t peek64(uint32_t q, uint32_t &bit64) const {
+    const uint32_t a = addr(q), sh = q & 31u;
+    const uint32_t w0 = lds32d(a), w1 = lds32d(a + 4), w2 = lds32d(a + 8);
+    bit64 = (w2 >> sh) & 1u;
+    return (uint64_t)__funnelshift_r(w0, w1, sh) | ((uint64_t)__funnelshift_r(w1, w2, sh) << 32);
+  }
+};
 
-// Decode one block into o[32], the block's 32 words in memory order.
+// Decode the block whose tag is at stage bit q into o[32] (the block's 32
+// words in memory order); q advances past the block. Plane codes are parsed
+// by a per-plane loop that is the same instruction stream for every lane
+// (the code class picks values by selects, not branches): each plane is
+// X_i, rebuilt to the pre-XOR plane P_i = X_i ^ P_{i+1} and stored in the
+// lane's row (FP32 plane i < 32 in word i; BF16 plane i < 16 in words i and
+// 16+i; DBX rows pre-shifted so row bit j is delta j). One 32x32 bit
+// transpose then turns rows into symbols. Returns false on a malformed code.
 template <bool W16>
-__device__ __forceinline__ bool decode_block(BitReader &br, uint32_t (&o)[32], uint32_t row, uint32_t lane) {
-  const uint32_t tag = br.get(3);
+__device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, uint32_t (&o)[32], uint32_t row,
+                                             uint32_t lane) {
+  constexpr int K = W16 ? 4 : 5;
+  const uint32_t tag = sb.peek32(q) & 7u;
+  q += 3;
   if (tag > kTagRAW) return false;
   if (tag == kTagRAW) {
-#pragma unroll 4
-    for (uint32_t k = 0; k < 32; ++k) sts32d(prow(row, lane, k), br.get(32));
 #pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = lds32d(prow(row, lane, k));
+    for (int k = 0; k < 32; ++k) o[k] = sb.peek32(q + 32u * k);
+    q += 1024;
     return true;
   }
   if (tag == kTagZVC) {
     if (W16) {
-      const uint32_t mlo = br.get(32), mhi = br.get(32);
+      const uint32_t mlo = sb.peek32(q), mhi = sb.peek32(q + 32);
+      q += 64;
 #pragma unroll 1
       for (uint32_t h = 0; h < 64; ++h) {
-        const uint32_t bit = (h < 32) ? (mlo >> h) : (mhi >> (h - 32));
-        sts16d(prow_half(row, lane, h), (bit & 1u) ? br.get(16) : 0u);
+        const uint32_t bit = ((h < 32) ? (mlo >> h) : (mhi >> (h - 32))) & 1u;
+        sts16d(prow_half(row, lane, h), bit ? (sb.peek32(q) & 0xFFFFu) : 0u);
+        q += bit * 16u;
       }
     } else {
-      const uint32_t mask = br.get(32);
+      const uint32_t mask = sb.peek32(q);
+      q += 32;
 #pragma unroll 1
-      for (uint32_t k = 0; k < 32; ++k) sts32d(prow(row, lane, k), ((mask >> k) & 1u) ? br.get(32) : 0u);
+      for (uint32_t k = 0; k < 32; ++k) {
+        const uint32_t bit = (mask >> k) & 1u;
+        sts32d(prow(row, lane, k), bit ? sb.peek32(q) : 0u);
+        q += bit * 32u;
+      }
     }
 #pragma unroll
     for (int k = 0; k < 32; ++k) o[k] = lds32d(prow(row, lane, k));
@@ -211,12 +132,17 @@ __device__ __forceinline__ bool decode_block(BitReader &br, uint32_t (&o)[32], u
   uint32_t basesym = 0, mlo = 0, mhi = 0;
   int top = W16 ? 15 : 31, W = W16 ? 64 : 32;
   if (tag == kTagDBX) {
-    basesym = br.get(W16 ? 16 : 32);
+    basesym = sb.peek32(q) & (W16 ? 0xFFFFu : 0xFFFFFFFFu);
+    q += W16 ? 16 : 32;
     ++top;
     --W;
   } else if (tag == kTagZBX) {
-    mlo = br.get(32);
-    if (W16) mhi = br.get(32);
+    mlo = sb.peek32(q);
+    q += 32;
+    if (W16) {
+      mhi = sb.peek32(q);
+      q += 32;
+    }
     W = __popc(mlo) + __popc(mhi);
     if (W == 0) {
 #pragma unroll
@@ -224,12 +150,51 @@ __device__ __forceinline__ bool decode_block(BitReader &br, uint32_t (&o)[32], u
       return true;
     }
   }
-  if (!parse_plane_rows<W16>(br, row, lane, top, W, ceil_log2_int(W), tag == kTagDBX)) return false;
+  const bool dbx = (tag == kTagDBX);
+  const uint32_t p = (uint32_t)ceil_log2_int(W);
+  const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
+  const uint32_t pmask = (1u << p) - 1u;
+  uint64_t Pup = 0;
+  int run = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (int i = top; i >= 0; --i) {
+    uint64_t X = 0;
+    if (run > 0) {
+      --run;
+    } else {
+      uint32_t b64;
+      const uint64_t win = sb.peek64(q, b64);
+      const uint32_t lo = (uint32_t)win;
+      const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // leading zero bits, capped at 4
+      const uint32_t qf = (lo >> 5) & pmask;
+      const bool hi4 = (lo & 16u) != 0;
+      const uint64_t xv = (W >= 64) ? ((win >> 1) | ((uint64_t)b64 << 63)) : ((win >> 1) & full);
+      const uint64_t xp = (hi4 ? 1ull : 3ull) << qf;
+      const uint64_t x5 = hi4 ? Pup : full;
+      X = (tz == 0u) ? xv : (tz == 3u) ? xp : (tz == 4u) ? x5 : 0ull;
+      q += (tz == 0u) ? 1u + (uint32_t)W : (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + p : 5u;
+      const int L = 2 + (int)((lo >> 2) & ((1u << K) - 1u));
+      if (tz == 1u) run = L - 1;
+      ok = ok && !(tz == 1u && L > i + 1) && !(tz == 3u && (int)qf + (hi4 ? 0 : 1) >= W) &&
+           !(tz == 4u && hi4 && i == top);
+    }
+    const uint64_t Pi = (i == top) ? X : (X ^ Pup);
+    Pup = Pi;
+    if (W16) {
+      if (i < 16) {
+        sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
+        sts32d(prow(row, lane, (uint32_t)i + 16), dbx ? (uint32_t)(Pi >> 31) : (uint32_t)(Pi >> 32));
+      }
+    } else if (i < 32) {
+      sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
+    }
+  }
 #pragma unroll
   for (int j = 0; j < 32; ++j) o[j] = lds32d(prow(row, lane, j));
   transpose32(o);  // FP32: o[j] = symbol j (or delta j); BF16: split words
   if (!W16) {
-    if (tag == kTagDBX) {
+    if (dbx) {
       o[0] = basesym;
 #pragma unroll
       for (int j = 1; j < 32; ++j) o[j] += o[j - 1];
@@ -243,10 +208,10 @@ __device__ __forceinline__ bool decode_block(BitReader &br, uint32_t (&o)[32], u
         o[k] = ((mlo >> k) & 1u) ? lds32d(prow(row, lane, rank)) : 0u;
       }
     }
-    return true;
+    return ok;
   }
   // BF16: o holds split words (word j = symbol j | symbol j+32 << 16)
-  if (tag == kTagDBX) {
+  if (dbx) {
     uint32_t prev = basesym;  // s_0
     o[0] = (o[0] & 0xFFFF0000u) | prev;
 #pragma unroll
@@ -282,7 +247,7 @@ __device__ __forceinline__ bool decode_block(BitReader &br, uint32_t (&o)[32], u
   for (int j = 0; j < 32; ++j) sp[j] = o[j];
 #pragma unroll
   for (int r = 0; r < 32; ++r) o[r] = raw_word_from_split(sp, r);
-  return true;
+  return ok;
 }
 
 // ------------------------------------------------------ block boundaries
@@ -549,6 +514,7 @@ template <bool W16>
 __global__ void __launch_bounds__(kDecWarps * 32, 2)
     decode_kernel(DecodeArgs p) {
   __shared__ __align__(16) uint32_t tile[kDecWarps][32 * 32];  // per warp: 32 lane rows of 128 B
+  __shared__ __align__(16) uint32_t stage[kDecWarps][kStageWords];  // per warp: the chunk's payload
   __shared__ uint16_t tail_starts[kDecWarps][32];
   const uint32_t lane = lane_id();
   const uint32_t warp = threadIdx.x >> 5;
@@ -618,15 +584,27 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
     return;
   }
 
+  // stage the payload: 16-byte units from a0 = off rounded down to 16
+  const uint64_t a0 = off & ~15ull;
+  const uint32_t nunits = (uint32_t)((off + L + 15 - a0) >> 4);
+  const uint32_t sbase = smem_u32(stage[warp]);
+  for (uint32_t u = lane; u < nunits; u += 32) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.in + a0) + u);
+    *reinterpret_cast<uint4 *>(&stage[warp][4 * u]) = v;
+  }
+  __syncwarp();
+  const StageBits sb{sbase};
+  const uint32_t bit0 = (uint32_t)(off - a0) * 8u;
+
   uint32_t *tw = tile[warp];
   const uint32_t row = smem_u32(tw) + lane * 128u;
   if (lane < nblk) {
-    BitReader br;
-    br.init(reinterpret_cast<const uint32_t *>(p.in), (p.comp_bytes + 3) / 4, 8ull * off + s0);
+    uint32_t q = bit0 + s0;
     uint32_t o[32];
-    ok = decode_block<W16>(br, o, row, lane);
-    if (lane + 1 < nblk && br.consumed != s1 - s0) ok = false;
-    if (lane + 1 == nblk && s0 + br.consumed > 8u * L) ok = false;
+    ok = decode_block<W16>(sb, q, o, row, lane);
+    const uint32_t used = q - bit0 - s0;
+    if (lane + 1 < nblk && used != s1 - s0) ok = false;
+    if (lane + 1 == nblk && s0 + used > 8u * L) ok = false;
 #pragma unroll
     for (int u = 0; u < 8; ++u)
       *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(tw) + tile_swz(lane, u)) =
