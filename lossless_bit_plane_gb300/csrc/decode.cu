@@ -152,44 +152,72 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
   }
   const bool dbx = (tag == kTagDBX);
   const uint32_t p = (uint32_t)ceil_log2_int(W);
-  const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
   const uint32_t pmask = (1u << p) - 1u;
-  uint64_t Pup = 0;
+  // code length by class (leading zero bits, capped at 4), 7 bits each
+  const uint32_t lens = (1u + (uint32_t)W) | ((2u + K) << 7) | (3u << 14) | ((5u + p) << 21);
+  // The walk kernel has already checked run lengths and the pre-XOR-zero
+  // code's plane; the position field's range is checked here.
+  bool bad = false;
   int run = 0;
-  bool ok = true;
+  if (!W16) {
+    const uint32_t full = (W >= 32) ? ~0u : ((1u << W) - 1u);
+    uint32_t Pup = 0;
 #pragma unroll 1
-  for (int i = top; i >= 0; --i) {
-    uint64_t X = 0;
-    if (run > 0) {
-      --run;
-    } else {
-      uint32_t b64;
-      const uint64_t win = sb.peek64(q, b64);
-      const uint32_t lo = (uint32_t)win;
-      const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // leading zero bits, capped at 4
-      const uint32_t qf = (lo >> 5) & pmask;
-      const bool hi4 = (lo & 16u) != 0;
-      const uint64_t xv = (W >= 64) ? ((win >> 1) | ((uint64_t)b64 << 63)) : ((win >> 1) & full);
-      const uint64_t xp = (hi4 ? 1ull : 3ull) << qf;
-      const uint64_t x5 = hi4 ? Pup : full;
-      X = (tz == 0u) ? xv : (tz == 3u) ? xp : (tz == 4u) ? x5 : 0ull;
-      q += (tz == 0u) ? 1u + (uint32_t)W : (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + p : 5u;
-      const int L = 2 + (int)((lo >> 2) & ((1u << K) - 1u));
-      if (tz == 1u) run = L - 1;
-      ok = ok && !(tz == 1u && L > i + 1) && !(tz == 3u && (int)qf + (hi4 ? 0 : 1) >= W) &&
-           !(tz == 4u && hi4 && i == top);
+    for (int i = top; i >= 0; --i) {
+      uint32_t X = 0;
+      if (run > 0) {
+        --run;
+      } else {
+        const uint32_t a = sb.addr(q), sh = q & 31u;
+        const uint32_t w0 = lds32d(a), w1 = lds32d(a + 4), w2 = lds32d(a + 8);
+        const uint32_t lo = __funnelshift_r(w0, w1, sh), hi = __funnelshift_r(w1, w2, sh);
+        const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;
+        const uint32_t qf = (lo >> 5) & pmask;
+        const bool hi4 = (lo & 16u) != 0;
+        const uint32_t xv = __funnelshift_r(lo, hi, 1) & full;
+        const uint32_t xp = (hi4 ? 1u : 3u) << qf;
+        const uint32_t x5 = hi4 ? Pup : full;
+        X = (tz == 0u) ? xv : (tz == 3u) ? xp : (tz == 4u) ? x5 : 0u;
+        q += (tz == 4u) ? 5u : ((lens >> (7u * tz)) & 127u);
+        if (tz == 1u) run = 1 + (int)((lo >> 2) & ((1u << K) - 1u));
+        bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
+      }
+      const uint32_t Pi = (i == top) ? X : (X ^ Pup);
+      Pup = Pi;
+      if (i < 32) sts32d(prow(row, lane, (uint32_t)i), dbx ? (Pi << 1) : Pi);
     }
-    const uint64_t Pi = (i == top) ? X : (X ^ Pup);
-    Pup = Pi;
-    if (W16) {
+  } else {
+    const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
+    uint64_t Pup = 0;
+#pragma unroll 1
+    for (int i = top; i >= 0; --i) {
+      uint64_t X = 0;
+      if (run > 0) {
+        --run;
+      } else {
+        uint32_t b64;
+        const uint64_t win = sb.peek64(q, b64);
+        const uint32_t lo = (uint32_t)win;
+        const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;
+        const uint32_t qf = (lo >> 5) & pmask;
+        const bool hi4 = (lo & 16u) != 0;
+        const uint64_t xv = (W >= 64) ? ((win >> 1) | ((uint64_t)b64 << 63)) : ((win >> 1) & full);
+        const uint64_t xp = (hi4 ? 1ull : 3ull) << qf;
+        const uint64_t x5 = hi4 ? Pup : full;
+        X = (tz == 0u) ? xv : (tz == 3u) ? xp : (tz == 4u) ? x5 : 0ull;
+        q += (tz == 4u) ? 5u : ((lens >> (7u * tz)) & 127u);
+        if (tz == 1u) run = 1 + (int)((lo >> 2) & ((1u << K) - 1u));
+        bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
+      }
+      const uint64_t Pi = (i == top) ? X : (X ^ Pup);
+      Pup = Pi;
       if (i < 16) {
         sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
         sts32d(prow(row, lane, (uint32_t)i + 16), dbx ? (uint32_t)(Pi >> 31) : (uint32_t)(Pi >> 32));
       }
-    } else if (i < 32) {
-      sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
     }
   }
+  const bool ok = !bad;
 #pragma unroll
   for (int j = 0; j < 32; ++j) o[j] = lds32d(prow(row, lane, j));
   transpose32(o);  // FP32: o[j] = symbol j (or delta j); BF16: split words

@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "pz_device.cuh"
 #include "pz_format.cuh"
@@ -302,14 +303,15 @@ __device__ __forceinline__ void emit_run(BitWriter &bw, int run, int K) {
     bw.put(2u | ((uint32_t)(run - 2) << 2), 2 + K);  // 0 1 + (run-2)
 }
 
-// One non-zero plane: the shortest applicable code, ties in the order
-// all-ones, pre-XOR-zero, two-adjacent, single-one, verbatim.
-__device__ __forceinline__ void emit_plane(BitWriter &bw, uint64_t X, bool prexor_zero, int W, int p,
-                                           uint64_t full) {
-  const int ones = __popcll(X);
-  const int q = __ffsll((long long)X) - 1;
+// One non-zero plane X (T = uint32_t for planes up to 32 bits, uint64_t up to
+// 64): the shortest applicable code, ties in the order all-ones,
+// pre-XOR-zero, two-adjacent, single-one, verbatim.
+template <typename T>
+__device__ __forceinline__ void emit_plane(BitWriter &bw, T X, bool prexor_zero, int W, int p, T full) {
+  const int ones = (sizeof(T) == 8) ? __popcll((uint64_t)X) : __popc((uint32_t)X);
+  const int q = (sizeof(T) == 8) ? (__ffsll((long long)X) - 1) : (__ffs((int)(uint32_t)X) - 1);
   const bool A = (X == full);
-  const bool T2 = (ones == 2) && ((X >> q) == 3ull);
+  const bool T2 = (ones == 2) && ((X >> q) == (T)3);
   const bool S1 = (ones == 1);
   int len = 1 + W;
   uint32_t val = 0;
@@ -318,11 +320,13 @@ __device__ __forceinline__ void emit_plane(BitWriter &bw, uint64_t X, bool prexo
   if (T2 && 5 + p <= len) { len = 5 + p; val = 8u | ((uint32_t)q << 5); verbatim = false; }   // 0 0 0 1 0 + q
   if (prexor_zero && 5 <= len) { len = 5; val = 16u; verbatim = false; }                        // 0 0 0 0 1
   if (A && 5 <= len) { len = 5; val = 0u; verbatim = false; }                                    // 0 0 0 0 0
-  if (verbatim) {
-    bw.put(1u, 1);  // 1 + the plane
-    bw.put64(X, (uint32_t)W);
-  } else {
+  if (!verbatim) {
     bw.put(val, (uint32_t)len);
+  } else if (sizeof(T) == 4 || W <= 32) {
+    bw.put_wide(((uint64_t)X << 1) | 1u, (uint32_t)W + 1);  // 1 + the plane
+  } else {
+    bw.put_wide(((uint64_t)(uint32_t)X << 1) | 1u, 33);
+    bw.put_wide((uint64_t)X >> 32, (uint32_t)W - 32);
   }
 }
 
@@ -332,26 +336,27 @@ __device__ __forceinline__ void emit_plane(BitWriter &bw, uint64_t X, bool prexo
 // q+1 needs a shift, and the top plane (the borrow plane) is passed in topv.
 template <bool W16>
 __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase, uint32_t lane, int top,
-                                               int W, int p, bool dbx, uint64_t topv) {
+                                                 int W, int p, bool dbx, uint64_t topv) {
+  using T = typename std::conditional<W16, uint64_t, uint32_t>::type;
   const int K = W16 ? 4 : 5;
-  const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
+  const T full = (W >= (int)(8 * sizeof(T))) ? ~(T)0 : (((T)1 << W) - 1);
   int run = 0;
-  uint64_t Pup = 0;
+  T Pup = 0;
 #pragma unroll 1
   for (int i = top; i >= 0; --i) {
-    uint64_t X;
+    T X;
     if (dbx && i == top) {
-      X = topv;
+      X = (T)topv;
     } else {
       const uint32_t lo = lds32(plane_row(rowbase, lane, (uint32_t)i));
       if (W16) {
         const uint32_t hi = lds32(plane_row(rowbase, lane, (uint32_t)i + 16));
-        X = dbx ? ((uint64_t)(lo >> 1) | ((uint64_t)hi << 31)) : ((uint64_t)lo | ((uint64_t)hi << 32));
+        X = (T)(dbx ? ((uint64_t)(lo >> 1) | ((uint64_t)hi << 31)) : ((uint64_t)lo | ((uint64_t)hi << 32)));
       } else {
-        X = dbx ? (uint64_t)(lo >> 1) : (uint64_t)lo;
+        X = (T)(dbx ? (lo >> 1) : lo);
       }
     }
-    const uint64_t P = (i == top) ? X : (X ^ Pup);
+    const T P = (i == top) ? X : (T)(X ^ Pup);
     if (X == 0) {
       ++run;
     } else {
@@ -359,7 +364,7 @@ __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase
         emit_run(bw, run, K);
         run = 0;
       }
-      emit_plane(bw, X, (i != top) && (P == 0), W, p, full);
+      emit_plane<T>(bw, X, (i != top) && (P == 0), W, p, full);
     }
     Pup = P;
   }

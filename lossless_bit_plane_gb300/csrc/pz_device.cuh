@@ -118,6 +118,23 @@ struct BitWriter {
       nacc -= 32;
     }
   }
+  // n <= 33 and v < 2^n (one or two words may complete)
+  __device__ __forceinline__ void put_wide(uint64_t v, uint32_t n) {
+    acc |= v << nacc;
+    nacc += n;
+    if (nacc >= 32) {
+      if (widx < cap) atomicOr(&buf[widx], (uint32_t)acc);
+      ++widx;
+      acc >>= 32;
+      nacc -= 32;
+      if (nacc >= 32) {
+        if (widx < cap) atomicOr(&buf[widx], (uint32_t)acc);
+        ++widx;
+        acc >>= 32;
+        nacc -= 32;
+      }
+    }
+  }
   __device__ __forceinline__ void put64(uint64_t v, uint32_t n) {  // n <= 64
     if (n > 32) {
       put((uint32_t)v, 32);
