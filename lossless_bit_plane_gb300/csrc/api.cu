@@ -45,8 +45,8 @@ cudaError_t device_info(DeviceInfo &out) {
   DeviceInfo &d = g_dev[dev];
   if (!d.ready) {
     if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const size_t smem = pz::encode_smem_bytes();
     for (int w = 0; w < 2; ++w) {
+      const size_t smem = pz::encode_smem_bytes(w == 1);
       const void *k = pz::encode_kernel_ptr(w == 1);
       if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
@@ -126,7 +126,7 @@ pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width, void *d_o
   if (grid > need) grid = need;
   void *args[2] = {&tmap, &a};
   if (cudaLaunchKernel(pz::encode_kernel_ptr(w16), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
-                       pz::encode_smem_bytes(), s) != cudaSuccess)
+                       pz::encode_smem_bytes(w16), s) != cudaSuccess)
     return PZ_ERR_CUDA;
   return PZ_OK;
 }
@@ -250,7 +250,7 @@ extern "C" pz_status pz_compress_noalloc(const void *d_in, size_t nbytes, int el
   if (grid > need) grid = need;
   void *args[2] = {&tmap, &a};
   if (cudaLaunchKernel(pz::encode_kernel_ptr(w16), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
-                       pz::encode_smem_bytes(), s) != cudaSuccess)
+                       pz::encode_smem_bytes(w16), s) != cudaSuccess)
     return PZ_ERR_CUDA;
   return PZ_OK;
 }

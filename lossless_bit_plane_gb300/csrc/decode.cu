@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(kWalkThreads)
 __device__ __forceinline__ uint32_t tile_swz(uint32_t r, uint32_t u) { return r * 128u + ((u ^ (r & 7u)) << 4); }
 
 template <bool W16>
-__global__ void __launch_bounds__(kDecWarps * 32, 2)
+__global__ void __launch_bounds__(kDecWarps * 32, 3)
     decode_kernel(DecodeArgs p) {
   __shared__ __align__(16) uint32_t tile[kDecWarps][32 * 32];  // per warp: 32 lane rows of 128 B
   __shared__ __align__(16) uint32_t stage[kDecWarps][kStageWords];  // per warp: the chunk's payload

@@ -84,10 +84,56 @@ __device__ __forceinline__ int single_plane_len(T X, T full, int W, int p) {
   return lv;
 }
 
+// Class of every plane of one candidate (bit i = plane i): non-zero, and the
+// code each non-zero plane takes: verbatim, a 5-bit code (all-ones or, if
+// not all-ones, pre-XOR-zero), or a 5+p-bit position code (single one or,
+// if not, two adjacent ones). FP32 DBX has a 33rd plane, whose six class
+// bits are packed in `top`.
+struct Plan {
+  uint32_t nz, v, f5, fa, m, ms;
+  uint32_t top;
+};
+
+// Shortest applicable code per non-zero plane of width W (position field
+// p), ties in the order all-ones, pre-XOR-zero, two-adjacent, single-one,
+// verbatim: 5-bit codes unless verbatim (1+W) is shorter, position codes
+// unless verbatim is shorter.
+__device__ __forceinline__ Plan make_plan(uint32_t NZ, uint32_t A, uint32_t PX, uint32_t S1, uint32_t T2, int W,
+                                          int p) {
+  const int lv = 1 + W, lm = 5 + p;
+  uint32_t f5 = (A | PX) & NZ;
+  uint32_t m = (S1 | T2) & NZ & ~f5;
+  if (5 > lv) f5 = 0;
+  if (lm > lv) m = 0;
+  Plan pl;
+  pl.nz = NZ;
+  pl.f5 = f5;
+  pl.fa = A & f5;
+  pl.m = m;
+  pl.ms = S1 & m;
+  pl.v = NZ & ~f5 & ~m;
+  pl.top = 0;
+  return pl;
+}
+
+__device__ __forceinline__ int plan_cost(const Plan &pl, int W, int p) {
+  return 5 * __popc(pl.f5) + (5 + p) * __popc(pl.m) + (1 + W) * __popc(pl.v);
+}
+
 struct Sizes {
   int s[5];
   uint32_t m0, m1;  // non-zero symbol masks: symbols 0..31 and (BF16) 32..63
+  uint32_t tag, bits;  // the kept candidate and its size (tag excluded)
+  Plan win;            // its plan (plane candidates only)
 };
+
+__device__ __forceinline__ void select_min(const Sizes &z, uint32_t &tag, uint32_t &bits);
+
+// Pick the smallest candidate (ties to the lowest tag) and keep its plan.
+__device__ __forceinline__ void keep_smallest(Sizes &z, const Plan &bx, const Plan &zbx, const Plan &dbx) {
+  select_min(z, z.tag, z.bits);
+  z.win = (z.tag == kTagZBX) ? zbx : (z.tag == kTagDBX) ? dbx : bx;
+}
 
 __device__ __forceinline__ void select_min(const Sizes &z, uint32_t &tag, uint32_t &bits) {
   tag = 0;
@@ -144,25 +190,29 @@ __device__ __forceinline__ Sizes classify32(const uint32_t (&s)[32]) {
   z.s[kTagZVC] = 32 + 32 * n;
   z.s[kTagRAW] = 1024;
   // BX: 32 planes of width 32, top plane 31
-  {
-    uint64_t NZ = a, PX = (~ors & a) & 0x7FFFFFFFu, ST = (a & ~b) | (b & ~c & adj);
-    z.s[kTagBX] = run_cost((uint32_t)~a, 5) + nonzero_cost(NZ, andx, PX, ST, 32, 5);
-  }
+  const uint32_t PX = (~ors & a) & 0x7FFFFFFFu;
+  const Plan bx = make_plan(a, andx, PX, a & ~b, b & ~c & adj, 32, 5);
+  z.s[kTagBX] = run_cost((uint32_t)~a, 5) + plan_cost(bx, 32, 5);
   // ZBX: mask + 32 planes of width n over the survivors
+  Plan zbx;
   if (n == 0) {
+    zbx = make_plan(0, 0, 0, 0, 0, 1, 0);
     z.s[kTagZBX] = 32;
   } else {
-    uint64_t NZ = a, PX = (~ors & a) & 0x7FFFFFFFu, ST = (a & ~b) | (b & ~c & adjz);
-    uint64_t A = ~zn & a;
-    z.s[kTagZBX] = 32 + run_cost((uint32_t)~a, 5) + nonzero_cost(NZ, A, PX, ST, n, ceil_log2_int(n));
+    const int pn = ceil_log2_int(n);
+    zbx = make_plan(a, ~zn & a, PX, a & ~b, b & ~c & adjz, n, pn);
+    z.s[kTagZBX] = 32 + run_cost((uint32_t)~a, 5) + plan_cost(zbx, n, pn);
   }
   // DBX: base + 33 planes of width 31 (plane 32 = borrow plane, the top)
+  Plan dbx = make_plan(ad, andd, ~ord & ad, ad & ~bd, bd & ~cd & adjd, 31, 5);
   {
-    uint64_t NZ = ad, PX = ~ord & ad, ST = (ad & ~bd) | (bd & ~cd & adjd);
-    uint64_t Z = (uint64_t)(uint32_t)~ad | ((uint64_t)(Bw == 0) << 32);
-    z.s[kTagDBX] = 32 + run_cost(Z, 5) + nonzero_cost(NZ, andd, PX, ST, 31, 5) +
-                   single_plane_len<uint32_t>(Bw, 0x7FFFFFFFu, 31, 5);
+    const int ones = __popc(Bw);
+    const Plan tp = make_plan(Bw != 0, Bw == 0x7FFFFFFFu, 0, ones == 1, ones == 2 && (Bw & (Bw >> 1)), 31, 5);
+    dbx.top = tp.nz | (tp.v << 1) | (tp.f5 << 2) | (tp.fa << 3) | (tp.m << 4) | (tp.ms << 5);
+    const uint64_t Z = (uint64_t)(uint32_t)~ad | ((uint64_t)(Bw == 0) << 32);
+    z.s[kTagDBX] = 32 + run_cost(Z, 5) + plan_cost(dbx, 31, 5) + plan_cost(tp, 31, 5);
   }
+  keep_smallest(z, bx, zbx, dbx);
   return z;
 }
 
@@ -232,35 +282,42 @@ __device__ __forceinline__ Sizes classify16(const uint32_t (&sp)[32]) {
   uint32_t ors16 = lo(ors) | hi(ors);
   uint32_t Z16 = ~a16 & 0xFFFFu;
   uint32_t PX16 = (~ors16 & a16) & 0x7FFFu;
+  Plan bx, zbx, dbx;
   // BX: 16 planes of width 64; adjacency across the half split is (31, 32)
   {
-    uint32_t adj16 = lo(adj) | hi(adj) | (lo(gprev) & hi(g0));
-    uint32_t and16 = lo(andx) & hi(andx);
-    uint64_t ST = (a16 & ~b16) | (b16 & ~c16 & adj16);
-    z.s[kTagBX] = run_cost(Z16, 4) + nonzero_cost(a16, and16, PX16, ST, 64, 6);
+    const uint32_t adj16 = lo(adj) | hi(adj) | (lo(gprev) & hi(g0));
+    const uint32_t and16 = lo(andx) & hi(andx);
+    bx = make_plan(a16, and16, PX16, a16 & ~b16, b16 & ~c16 & adj16, 64, 6);
+    z.s[kTagBX] = run_cost(Z16, 4) + plan_cost(bx, 64, 6);
   }
   if (n == 0) {
+    zbx = make_plan(0, 0, 0, 0, 0, 1, 0);
     z.s[kTagZBX] = 64;
   } else {
-    uint32_t adjz16 = lo(adjz) | hi(adjz) | (lo(last) & hi(fst));
-    uint32_t A = ~(lo(zn) | hi(zn)) & a16;
-    uint64_t ST = (a16 & ~b16) | (b16 & ~c16 & adjz16);
-    z.s[kTagZBX] = 64 + run_cost(Z16, 4) + nonzero_cost(a16, A, PX16, ST, n, ceil_log2_int(n));
+    const uint32_t adjz16 = lo(adjz) | hi(adjz) | (lo(last) & hi(fst));
+    const uint32_t A = ~(lo(zn) | hi(zn)) & a16;
+    const int pn = ceil_log2_int(n);
+    zbx = make_plan(a16, A, PX16, a16 & ~b16, b16 & ~c16 & adjz16, n, pn);
+    z.s[kTagZBX] = 64 + run_cost(Z16, 4) + plan_cost(zbx, n, pn);
   }
-  // DBX: base + 17 planes of width 63 (plane 16 = borrow plane)
+  // DBX: base + 17 planes of width 63 (plane 16 = borrow plane, the top)
   {
-    uint32_t ad16 = lo(ad) | hi(ad);
-    uint32_t bd16 = lo(bd) | hi(bd) | (lo(ad) & hi(ad));
-    uint32_t cd16 = lo(cd) | hi(cd) | (lo(ad) & hi(bd)) | (lo(bd) & hi(ad));
-    uint32_t adjd16 = lo(adjd) | hi(adjd) | (lo(gdprev) & hi(gd0));
-    uint32_t andd16 = lo(andd) & hi(andd);
-    uint32_t ord16 = lo(ord) | hi(ord);
-    uint64_t Bp = (uint64_t)Blo | ((uint64_t)Bhi << 32);
-    uint64_t ST = (ad16 & ~bd16) | (bd16 & ~cd16 & adjd16);
-    uint64_t Z = (~ad16 & 0xFFFFu) | ((uint64_t)(Bp == 0) << 16);
-    z.s[kTagDBX] = 16 + run_cost(Z, 4) + nonzero_cost(ad16, andd16, ~ord16 & ad16, ST, 63, 6) +
-                   single_plane_len<uint64_t>(Bp, (1ull << 63) - 1, 63, 6);
+    const uint32_t ad16 = lo(ad) | hi(ad);
+    const uint32_t bd16 = lo(bd) | hi(bd) | (lo(ad) & hi(ad));
+    const uint32_t cd16 = lo(cd) | hi(cd) | (lo(ad) & hi(bd)) | (lo(bd) & hi(ad));
+    const uint32_t adjd16 = lo(adjd) | hi(adjd) | (lo(gdprev) & hi(gd0));
+    const uint32_t andd16 = lo(andd) & hi(andd);
+    const uint32_t ord16 = lo(ord) | hi(ord);
+    const uint64_t Bp = (uint64_t)Blo | ((uint64_t)Bhi << 32);
+    const int bones = __popcll(Bp);
+    const uint32_t tnz = (Bp != 0), tA = (Bp == (1ull << 63) - 1), tS = (bones == 1),
+                   tT = (bones == 2) && ((Bp & (Bp >> 1)) != 0);
+    dbx = make_plan(ad16 | (tnz << 16), andd16 | (tA << 16), ~ord16 & ad16, (ad16 & ~bd16) | (tS << 16),
+                    (bd16 & ~cd16 & adjd16) | (tT << 16), 63, 6);
+    const uint32_t Z = ~dbx.nz & 0x1FFFFu;
+    z.s[kTagDBX] = 16 + run_cost(Z, 4) + plan_cost(dbx, 63, 6);
   }
+  keep_smallest(z, bx, zbx, dbx);
   return z;
 }
 
@@ -330,50 +387,69 @@ __device__ __forceinline__ void emit_plane(BitWriter &bw, T X, bool prexor_zero,
   }
 }
 
-// Plane codes, top plane first. Plane i < 32 (FP32) or < 16 (BF16, low and
-// high 32 symbols in rows i and 16+i) comes from the transposed rows; for
+// Plane codes, top plane first, driven by the candidate's plan: a zero
+// plane starts a run that extends to the next non-zero plane (found with a
+// leading-zero count), a 5-bit code needs no plane data, and only verbatim
+// and position codes read the plane. Plane i < 32 (FP32) or < 16 (BF16, low
+// and high 32 symbols in rows i and 16+i) comes from the transposed rows; for
 // DBX the rows hold deltas at bit j = delta index j, so plane bit q = delta
 // q+1 needs a shift, and the top plane (the borrow plane) is passed in topv.
 template <bool W16>
 __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase, uint32_t lane, int top,
-                                                 int W, int p, bool dbx, uint64_t topv) {
-  using T = typename std::conditional<W16, uint64_t, uint32_t>::type;
-  const int K = W16 ? 4 : 5;
-  const T full = (W >= (int)(8 * sizeof(T))) ? ~(T)0 : (((T)1 << W) - 1);
-  int run = 0;
-  T Pup = 0;
+                                                 int W, int p, bool dbx, uint64_t topv, const Plan &pl) {
+  constexpr int K = W16 ? 4 : 5;
+  const bool wide_top = !W16 && dbx;  // FP32 DBX: plane 32 lives in pl.top
+  auto widen = [&](uint32_t m, int k) -> uint64_t {
+    return (uint64_t)m | (wide_top ? ((uint64_t)((pl.top >> k) & 1u) << 32) : 0ull);
+  };
+  const uint64_t NZ = widen(pl.nz, 0), V = widen(pl.v, 1), F5 = widen(pl.f5, 2), FA = widen(pl.fa, 3),
+                 MS = widen(pl.ms, 5);
+  const uint32_t lm = 5u + (uint32_t)p;
+  int i = top;
 #pragma unroll 1
-  for (int i = top; i >= 0; --i) {
-    T X;
-    if (dbx && i == top) {
-      X = (T)topv;
+  while (i >= 0) {
+    const uint64_t bit = 1ull << i;
+    if (!(NZ & bit)) {  // zero planes i .. hb+1
+      const uint64_t below = NZ & (bit - 1);
+      const int hb = below ? 63 - __clzll((long long)below) : -1;
+      emit_run(bw, i - hb, K);
+      i = hb;
+      continue;
+    }
+    if (F5 & bit) {
+      bw.put((FA & bit) ? 0u : 16u, 5);  // 0 0 0 0 0 all ones / 0 0 0 0 1 pre-XOR plane zero
     } else {
-      const uint32_t lo = lds32(plane_row(rowbase, lane, (uint32_t)i));
-      if (W16) {
-        const uint32_t hi = lds32(plane_row(rowbase, lane, (uint32_t)i + 16));
-        X = (T)(dbx ? ((uint64_t)(lo >> 1) | ((uint64_t)hi << 31)) : ((uint64_t)lo | ((uint64_t)hi << 32)));
+      uint64_t X;
+      if (dbx && i == top) {
+        X = topv;
       } else {
-        X = (T)(dbx ? (lo >> 1) : lo);
+        const uint32_t lo = lds32(plane_row(rowbase, lane, (uint32_t)i));
+        if (W16) {
+          const uint32_t hi = lds32(plane_row(rowbase, lane, (uint32_t)i + 16));
+          X = dbx ? ((uint64_t)(lo >> 1) | ((uint64_t)hi << 31)) : ((uint64_t)lo | ((uint64_t)hi << 32));
+        } else {
+          X = dbx ? (uint64_t)(lo >> 1) : (uint64_t)lo;
+        }
+      }
+      if (V & bit) {  // 1 + the plane
+        if (W <= 32) {
+          bw.put_wide((X << 1) | 1u, (uint32_t)W + 1);
+        } else {
+          bw.put_wide(((X & 0xFFFFFFFFull) << 1) | 1u, 33);
+          bw.put_wide(X >> 32, (uint32_t)W - 32);
+        }
+      } else {  // 0 0 0 1 1 + q single one / 0 0 0 1 0 + q two adjacent ones
+        const uint32_t q = (uint32_t)(__ffsll((long long)X) - 1);
+        bw.put(((MS & bit) ? 24u : 8u) | (q << 5), lm);
       }
     }
-    const T P = (i == top) ? X : (T)(X ^ Pup);
-    if (X == 0) {
-      ++run;
-    } else {
-      if (run) {
-        emit_run(bw, run, K);
-        run = 0;
-      }
-      emit_plane<T>(bw, X, (i != top) && (P == 0), W, p, full);
-    }
-    Pup = P;
+    --i;
   }
-  if (run) emit_run(bw, run, K);
 }
 
 // FP32 emit of the chosen candidate. s: the block's symbols; nz: non-zero mask.
 __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, const uint32_t (&s)[32], uint32_t nz,
-                                      uint32_t rowbase, uint32_t lane) {
+                                      uint32_t rowbase, uint32_t lane, const Plan &pl) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -419,13 +495,13 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, const uint32
   transpose32(T);
 #pragma unroll
   for (int i = 0; i < 32; ++i) sts32(plane_row(rowbase, lane, i), T[i]);
-  emit_plane_codes<false>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv);
+  emit_plane_codes<false>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv, pl);
 }
 
 // BF16 emit of the chosen candidate. sp: split-packed symbols (word j =
 // symbol j | symbol j+32 << 16); mlo/mhi: non-zero masks of 0..31 / 32..63.
 __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, const uint32_t (&sp)[32], uint32_t mlo,
-                                      uint32_t mhi, uint32_t rowbase, uint32_t lane) {
+                                      uint32_t mhi, uint32_t rowbase, uint32_t lane, const Plan &pl) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -489,7 +565,7 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, const uint32
   transpose32(T);
 #pragma unroll
   for (int i = 0; i < 32; ++i) sts32(plane_row(rowbase, lane, i), T[i]);
-  emit_plane_codes<true>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv);
+  emit_plane_codes<true>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv, pl);
 }
 
 // --------------------------------------------------------------- look-back
@@ -569,12 +645,17 @@ __device__ __forceinline__ void copy_out(const uint32_t *buf, uint32_t L, uint8_
 constexpr int kEncWarps = 8;
 constexpr int kOutWords = 1024 + 4;
 
-struct EncSmem {
-  // per warp: stage[2][4096] (1024-aligned), outbuf[kOutWords], mbar[2]
-  static constexpr size_t kStageBytes = 2 * 4096;
+// Shared memory per warp: NSTAGE 4 KB stage buffers (1024-aligned, the TMA
+// destination), the chunk's output word buffer, two mbarriers. FP32 runs one
+// stage at three CTAs per SM (24 warps); BF16, whose classifier needs more
+// registers, runs two stages (the next chunk's load in flight) at two CTAs.
+template <bool W16>
+struct EncCfg {
+  static constexpr int kStages = W16 ? 2 : 1;
+  static constexpr int kMinCtas = W16 ? 2 : 3;
+  static constexpr size_t kStageBytes = kStages * 4096;
   static constexpr size_t kOutBytes = kOutWords * 4;
-  static constexpr size_t kBytes =
-      1024 + kEncWarps * kStageBytes + kEncWarps * kOutBytes + kEncWarps * 16;
+  static constexpr size_t kBytes = 1024 + kEncWarps * kStageBytes + kEncWarps * kOutBytes + kEncWarps * 16;
 };
 
 // Byte address of 16-byte unit u of row r in a 128-byte-swizzled stage.
@@ -583,18 +664,17 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t u) {
 }
 
 template <bool W16>
-__global__ void __launch_bounds__(kEncWarps * 32, 2)
+__global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     encode_kernel(const __grid_constant__ CUtensorMap tmap, EncodeArgs p) {
+  using Cfg = EncCfg<W16>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t lane = lane_id();
   const uint32_t warp = threadIdx.x >> 5;
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  uint8_t *stage0 = base + warp * EncSmem::kStageBytes;
-  uint32_t *outbuf = reinterpret_cast<uint32_t *>(base + kEncWarps * EncSmem::kStageBytes +
-                                                  warp * EncSmem::kOutBytes);
-  uint64_t *mbar = reinterpret_cast<uint64_t *>(base + kEncWarps * EncSmem::kStageBytes +
-                                                kEncWarps * EncSmem::kOutBytes) +
+  uint8_t *stage0 = base + warp * Cfg::kStageBytes;
+  uint32_t *outbuf = reinterpret_cast<uint32_t *>(base + kEncWarps * Cfg::kStageBytes + warp * Cfg::kOutBytes);
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(base + kEncWarps * Cfg::kStageBytes + kEncWarps * Cfg::kOutBytes) +
                    2 * warp;
   const uint32_t mb[2] = {smem_u32(mbar), smem_u32(mbar + 1)};
   if (lane == 0) {
@@ -645,7 +725,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, 2)
     uint32_t nt = 0;
     if (lane == 0) nt = atomicAdd(p.ticket, 1u);
     nt = __shfl_sync(0xFFFFFFFFu, nt, 0);
-    if (nt < C) issue(nt, cur ^ 1);
+    if (Cfg::kStages == 2 && nt < C) issue(nt, cur ^ 1);  // prefetch the next chunk
 
     uint8_t *st = stage0 + cur * 4096;
     if (uses_tma(t)) {
@@ -677,8 +757,8 @@ __global__ void __launch_bounds__(kEncWarps * 32, 2)
       for (int j = 0; j < 32; ++j) s[j] = split_word(raw, j);
     }
     Sizes z = W16 ? classify16(s) : classify32(s);
-    uint32_t tag, bits;
-    select_min(z, tag, bits);
+    const uint32_t tag = z.tag;
+    uint32_t bits = z.bits;
     bits = active ? bits + 3 : 0;
 
     // block bit offsets: warp prefix sum
@@ -704,10 +784,11 @@ __global__ void __launch_bounds__(kEncWarps * 32, 2)
         bw.init(outbuf, off, kOutWords);
         bw.put(tag, 3);
         const uint32_t rowbase = smem_u32(st) + lane * 128u;
+        const Plan &pl = z.win;
         if (W16)
-          emit16(bw, tag, s, z.m0, z.m1, rowbase, lane);
+          emit16(bw, tag, s, z.m0, z.m1, rowbase, lane, pl);
         else
-          emit32(bw, tag, s, z.m0, rowbase, lane);
+          emit32(bw, tag, s, z.m0, rowbase, lane, pl);
         bw.flush();
       }
     } else {
@@ -730,7 +811,10 @@ __global__ void __launch_bounds__(kEncWarps * 32, 2)
     __syncwarp();
     fence_proxy_async_smem();  // generic-proxy use of the stage before the next TMA write
     t = nt;
-    cur ^= 1;
+    if (Cfg::kStages == 2)
+      cur ^= 1;
+    else if (t < C)
+      issue(t, cur);  // one stage: load the next chunk now that this one is done
   }
   if (failed && lane == 0) atomicMax(p.total, ~0ull);
 }
@@ -738,7 +822,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, 2)
 template __global__ void encode_kernel<false>(const __grid_constant__ CUtensorMap, EncodeArgs);
 template __global__ void encode_kernel<true>(const __grid_constant__ CUtensorMap, EncodeArgs);
 
-size_t encode_smem_bytes() { return EncSmem::kBytes; }
+size_t encode_smem_bytes(bool w16) { return w16 ? EncCfg<true>::kBytes : EncCfg<false>::kBytes; }
 int encode_threads() { return kEncWarps * 32; }
 int encode_warps() { return kEncWarps; }
 

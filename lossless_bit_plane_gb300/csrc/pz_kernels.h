@@ -28,7 +28,7 @@ struct DecodeArgs {
   uint32_t num_chunks;
 };
 
-size_t encode_smem_bytes();
+size_t encode_smem_bytes(bool w16);
 int encode_threads();
 int encode_warps();
 const void *encode_kernel_ptr(bool w16);
