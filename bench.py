@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--cpu-sample-mib", type=float, default=4.0,
                     help="MiB per segment timed through the CPU oracle")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="sweep",
+                    help="'sweep' (the 1 GiB sweep, the headline) or one sweep segment as <kind>_<dtype>, "
+                         "e.g. attention_fp32, conv_bf16, random_u32 (used for small profiling cases)")
     return ap.parse_args()
 
 
@@ -152,10 +155,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload
 
-def make_workload():
+def make_workload(name: str = "sweep"):
     from lossless_bit_plane_gb300 import workloads as W
 
-    return W.sweep_1gib()
+    if name == "sweep":
+        return W.sweep_1gib()
+    kind, dtype = name.rsplit("_", 1)
+    return [W.sweep_segment(kind, dtype)]
+
+
+def workload_label(name: str) -> str:
+    return WORKLOAD if name == "sweep" else f"one 1 GiB-sweep segment: {name}"
 
 
 def peak_hbm():
@@ -195,7 +205,7 @@ def cpu_oracle_sample(segs, mib: float):
 def run_reference(args, rank: int):
     if rank != 0:
         return 0
-    segs = make_workload()
+    segs = make_workload(args.workload)
     mib = min(args.cpu_sample_mib, 1.0)
     for _ in range(args.warmup):
         cpu_oracle_sample(segs, mib)
@@ -211,7 +221,7 @@ def run_reference(args, rank: int):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (tc_tot + td_tot) / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "data": "synthetic", "config": {"workload": workload_label(args.workload), "sample": sample},
         "compress_gbs": nb_tot / tc_tot / 1e9, "decompress_gbs": nb_tot / td_tot / 1e9,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -233,7 +243,7 @@ def run_ours(args, rank: int, world: int, local: int):
     build.build()
     _lib.load()
 
-    segs = make_workload()
+    segs = make_workload(args.workload)
     stream = torch.cuda.current_stream(dev)
     d_in = [torch.from_numpy(t.data).to(dev) for t in segs]
     d_out = [torch.empty(_lib.pz_max_compressed_bytes(t.nbytes), dtype=torch.uint8, device=dev) for t in segs]
@@ -344,7 +354,7 @@ def run_ours(args, rank: int, world: int, local: int):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "bytes_per_step_per_gpu": raw, "parallelism": f"replicas x{world}",
+        "config": {"workload": workload_label(args.workload), "bytes_per_step_per_gpu": raw, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (128-256 MiB per call); no flush",
                    "sha256": {t.name: __import__("lossless_bit_plane_gb300.workloads", fromlist=["x"]).sha256(t.data)[:16]
                               for t in segs}},

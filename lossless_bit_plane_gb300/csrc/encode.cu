@@ -147,15 +147,50 @@ __device__ __forceinline__ void select_min(const Sizes &z, uint32_t &tag, uint32
   bits = (uint32_t)best;
 }
 
+// The lane's block in its 128-byte row of the stage, as the TMA left it
+// (16-byte units swizzled by row): unit u holds words 4u .. 4u+3.
+__device__ __forceinline__ uint4 stage_unit(uint32_t rowbase, uint32_t r, uint32_t u) {
+  uint4 q;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+               : "r"(rowbase + ((u ^ (r & 7u)) << 4))
+               : "memory");
+  return q;
+}
+__device__ __forceinline__ uint32_t unit_word(const uint4 &q, int k) {
+  return (k == 0) ? q.x : (k == 1) ? q.y : (k == 2) ? q.z : q.w;
+}
+// The block's 32 words into registers (FP32), or its split-packed words
+// (BF16: word j = symbol j | symbol j+32 << 16).
+template <bool W16>
+__device__ __forceinline__ void load_block(uint32_t rowbase, uint32_t lane, uint32_t (&s)[32]) {
+  uint32_t raw[32];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 q = stage_unit(rowbase, lane, u);
+    raw[4 * u] = q.x;
+    raw[4 * u + 1] = q.y;
+    raw[4 * u + 2] = q.z;
+    raw[4 * u + 3] = q.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) s[j] = W16 ? split_word(raw, j) : raw[j];
+}
+
 // ------------------------------------------------------------ FP32 classify
 // s: the block's 32 symbols. Returns the five candidate sizes (tag excluded).
-__device__ __forceinline__ Sizes classify32(const uint32_t (&s)[32]) {
+// The words are streamed from the stage row four at a time, so that only the
+// accumulators stay in registers.
+__device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0;  // BX
   uint32_t nz = 0, zn = 0, adjz = 0, last = 0;                            // ZBX / ZVC
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Bw = 0, gdprev = 0;  // DBX
+  uint32_t xprev = 0;
+  uint4 q = make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int k = 0; k < 32; ++k) {
-    uint32_t x = s[k];
+    if ((k & 3) == 0) q = stage_unit(rowbase, lane, (uint32_t)(k >> 2));
+    const uint32_t x = unit_word(q, k & 3);
     uint32_t g = x ^ (x >> 1);
     ors |= x;
     c |= b & g;
@@ -170,7 +205,7 @@ __device__ __forceinline__ Sizes classify32(const uint32_t (&s)[32]) {
     adjz |= last & g;
     last = x ? g : last;
     if (k) {
-      uint64_t d = (uint64_t)x - (uint64_t)s[k - 1];
+      uint64_t d = (uint64_t)x - (uint64_t)xprev;
       uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);  // hi: borrow mask
       uint32_t gd = lo ^ __funnelshift_r(lo, hi, 1);
       ord |= lo;
@@ -182,6 +217,7 @@ __device__ __forceinline__ Sizes classify32(const uint32_t (&s)[32]) {
       andd &= gd;
       gdprev = gd;
     }
+    xprev = x;
   }
   Sizes z;
   z.m0 = nz;
@@ -218,15 +254,23 @@ __device__ __forceinline__ Sizes classify32(const uint32_t (&s)[32]) {
 
 // ------------------------------------------------------------ BF16 classify
 // sp: split-packed block (word j = symbol j | symbol j+32 << 16).
-__device__ __forceinline__ Sizes classify16(const uint32_t (&sp)[32]) {
+// Split-packed words (word j = symbol j | symbol j+32 << 16) are built while
+// streaming the stage row: word j needs raw words j/2 and 16 + j/2.
+__device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane) {
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0, g0 = 0;
   uint32_t mlo = 0, mhi = 0, zn = 0, adjz = 0, last = 0, fst = 0, seen = 0;
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Blo = 0, Bhi = 0, gdprev = 0,
            gd0 = 0;
-  const uint32_t s31lo = sp[31] << 16;  // symbol 31 moved to the high half
+  const uint32_t s31lo = stage_unit(rowbase, lane, 3).w & 0xFFFF0000u;  // symbol 31 in the high half
+  uint32_t xprev = 0;
+  uint4 qa = make_uint4(0, 0, 0, 0), qb = make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    uint32_t x = sp[j];
+    if ((j & 7) == 0) {
+      qa = stage_unit(rowbase, lane, (uint32_t)(j >> 3));
+      qb = stage_unit(rowbase, lane, 4u + (uint32_t)(j >> 3));
+    }
+    const uint32_t x = prmt(unit_word(qa, (j >> 1) & 3), unit_word(qb, (j >> 1) & 3), (j & 1) ? 0x7632u : 0x5410u);
     uint32_t g = x ^ ((x >> 1) & 0x7FFF7FFFu);
     ors |= x;
     c |= b & g;
@@ -246,7 +290,7 @@ __device__ __forceinline__ Sizes classify16(const uint32_t (&sp)[32]) {
     seen |= m;
     // DBX: lo half d_j = s_j - s_{j-1} (j >= 1), hi half d_{j+32} = s_{j+32} - s_{j+31}
     uint32_t bo;
-    uint32_t d = sub16x2(x, j ? sp[j - 1] : s31lo, bo);
+    uint32_t d = sub16x2(x, j ? xprev : s31lo, bo);
     if (j == 0) {
       d &= 0xFFFF0000u;
       bo &= 0x80000000u;
@@ -266,6 +310,7 @@ __device__ __forceinline__ Sizes classify16(const uint32_t (&sp)[32]) {
       Blo |= ((bo >> 15) & 1u) << (j - 1);  // d_j -> position j-1
       Bhi |= (bo >> 31) << (j - 1);         // d_{j+32} -> position j+31
     }
+    xprev = x;
   }
   // combine the two halves (symbols 0..31 and 32..63) into 16-plane masks
   auto lo = [](uint32_t v) { return v & 0xFFFFu; };
@@ -448,8 +493,8 @@ __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase
 }
 
 // FP32 emit of the chosen candidate. s: the block's symbols; nz: non-zero mask.
-__device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, const uint32_t (&s)[32], uint32_t nz,
-                                      uint32_t rowbase, uint32_t lane, const Plan &pl) {
+__device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t nz, uint32_t rowbase, uint32_t lane,
+                                      const Plan &pl) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -475,6 +520,8 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, const uint32
       T[j] = t ^ (t >> 1);
     }
   } else if (tag == kTagDBX) {
+    uint32_t s[32];
+    load_block<false>(rowbase, lane, s);
     bw.put(s[0], 32);
     uint32_t Bw = 0;
     T[0] = 0;
@@ -489,8 +536,9 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, const uint32
     top = 32;
     W = 31;
   } else {
+    load_block<false>(rowbase, lane, T);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) T[j] = s[j] ^ (s[j] >> 1);
+    for (int j = 0; j < 32; ++j) T[j] ^= T[j] >> 1;
   }
   transpose32(T);
 #pragma unroll
@@ -500,8 +548,8 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, const uint32
 
 // BF16 emit of the chosen candidate. sp: split-packed symbols (word j =
 // symbol j | symbol j+32 << 16); mlo/mhi: non-zero masks of 0..31 / 32..63.
-__device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, const uint32_t (&sp)[32], uint32_t mlo,
-                                      uint32_t mhi, uint32_t rowbase, uint32_t lane, const Plan &pl) {
+__device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t mlo, uint32_t mhi, uint32_t rowbase,
+                                      uint32_t lane, const Plan &pl) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -538,6 +586,8 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, const uint32
       T[j] = t ^ ((t >> 1) & 0x7FFF7FFFu);
     }
   } else if (tag == kTagDBX) {
+    uint32_t sp[32];
+    load_block<true>(rowbase, lane, sp);
     bw.put(sp[0] & 0xFFFFu, 16);
     const uint32_t s31lo = sp[31] << 16;
     uint32_t Blo = 0, Bhi = 0;
@@ -559,8 +609,9 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, const uint32
     top = 16;
     W = 63;
   } else {
+    load_block<true>(rowbase, lane, T);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) T[j] = sp[j] ^ ((sp[j] >> 1) & 0x7FFF7FFFu);
+    for (int j = 0; j < 32; ++j) T[j] ^= (T[j] >> 1) & 0x7FFF7FFFu;
   }
   transpose32(T);
 #pragma unroll
@@ -739,24 +790,8 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     const uint32_t nblk = (raw_len + 127u) >> 7;
     const bool active = lane < nblk;
 
-    // the lane's block, 8 x 16 B from its swizzled row
-    uint32_t s[32];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      uint4 q = *reinterpret_cast<const uint4 *>(st + swz(lane, u));
-      s[4 * u] = q.x;
-      s[4 * u + 1] = q.y;
-      s[4 * u + 2] = q.z;
-      s[4 * u + 3] = q.w;
-    }
-    if (W16) {
-      uint32_t raw[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) raw[k] = s[k];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) s[j] = split_word(raw, j);
-    }
-    Sizes z = W16 ? classify16(s) : classify32(s);
+    const uint32_t rowbase = smem_u32(st) + lane * 128u;
+    Sizes z = W16 ? classify16(rowbase, lane) : classify32(rowbase, lane);
     const uint32_t tag = z.tag;
     uint32_t bits = z.bits;
     bits = active ? bits + 3 : 0;
@@ -783,12 +818,11 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
         BitWriter bw;
         bw.init(outbuf, off, kOutWords);
         bw.put(tag, 3);
-        const uint32_t rowbase = smem_u32(st) + lane * 128u;
         const Plan &pl = z.win;
         if (W16)
-          emit16(bw, tag, s, z.m0, z.m1, rowbase, lane, pl);
+          emit16(bw, tag, z.m0, z.m1, rowbase, lane, pl);
         else
-          emit32(bw, tag, s, z.m0, rowbase, lane, pl);
+          emit32(bw, tag, z.m0, rowbase, lane, pl);
         bw.flush();
       }
     } else {
