@@ -696,14 +696,15 @@ __device__ __forceinline__ void copy_out(const uint32_t *buf, uint32_t L, uint8_
 constexpr int kEncWarps = 8;
 constexpr int kOutWords = 1024 + 4;
 
-// Shared memory per warp: NSTAGE 4 KB stage buffers (1024-aligned, the TMA
-// destination), the chunk's output word buffer, two mbarriers. FP32 runs one
-// stage at three CTAs per SM (24 warps); BF16, whose classifier needs more
-// registers, runs two stages (the next chunk's load in flight) at two CTAs.
+// Shared memory per warp: kStages 4 KB stage buffers (1024-aligned, the TMA
+// destination), the chunk's output word buffer, two mbarriers. One stage at
+// three CTAs per SM (24 warps): the next chunk is loaded after this one is
+// done, and the other warps cover that load's latency. (Two stages, with the
+// next chunk's load in flight, need more shared memory than three CTAs allow.)
 template <bool W16>
 struct EncCfg {
-  static constexpr int kStages = W16 ? 2 : 1;
-  static constexpr int kMinCtas = W16 ? 2 : 3;
+  static constexpr int kStages = 1;
+  static constexpr int kMinCtas = 3;
   static constexpr size_t kStageBytes = kStages * 4096;
   static constexpr size_t kOutBytes = kOutWords * 4;
   static constexpr size_t kBytes = 1024 + kEncWarps * kStageBytes + kEncWarps * kOutBytes + kEncWarps * 16;
