@@ -357,6 +357,13 @@ struct RingReader {
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hi) : "r"(ring + (((w + 1) & (kRingUnits * 4 - 1)) << 2)) : "memory");
     return __funnelshift_r(lo, hi, q & 31u);
   }
+  // the single bit at chunk bit pos (resident)
+  __device__ __forceinline__ uint32_t bit_resident(uint32_t pos) const {
+    const uint32_t q = bit0 + pos;
+    uint32_t w;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(ring + (((q >> 5) & (kRingUnits * 4 - 1)) << 2)) : "memory");
+    return (w >> (q & 31u)) & 1u;
+  }
   // make every peek at or below pos resident
   __device__ __forceinline__ void ensure(uint32_t pos) {
     const uint32_t q = bit0 + pos;
@@ -372,11 +379,12 @@ struct WindowPeeker {  // adapts WindowReader to the ensure / peek_resident inte
   WindowReader r;
   __device__ __forceinline__ void ensure(uint32_t) const {}
   __device__ __forceinline__ uint32_t peek_resident(uint32_t pos) const { return r.peek(pos); }
+  __device__ __forceinline__ uint32_t bit_resident(uint32_t pos) const { return r.peek(pos) & 1u; }
   __device__ __forceinline__ uint32_t peek(uint32_t pos) const { return r.peek(pos); }
 };
 
 // Advance pos over the plane codes of planes top..0 of width W. Each step
-// tests the flag bit of the next four codes under the assumption that they
+// tests the flag bits of the next eight codes under the assumption that they
 // are verbatim (a verbatim code is 1 + W bits): a run of m leading verbatim
 // codes advances m planes at once; otherwise the code at pos is classified
 // by its leading zero bits (stream order, capped at 4): 01 run (2+K bits,
@@ -384,6 +392,7 @@ struct WindowPeeker {  // adapts WindowReader to the ensure / peek_resident inte
 // all-ones / pre-XOR-zero (5).
 template <typename Reader>
 __device__ __forceinline__ bool walk_planes(Reader &rd, uint32_t &pos, int top, int W, int K) {
+  constexpr int kSkip = 8;
   const uint32_t p = (uint32_t)ceil_log2_int(W);
   const uint32_t S = 1u + (uint32_t)W;
   const uint32_t kmask = (1u << K) - 1u;
@@ -391,17 +400,18 @@ __device__ __forceinline__ bool walk_planes(Reader &rd, uint32_t &pos, int top, 
   bool ok = true;
 #pragma unroll 1
   while (i >= 0) {
-    rd.ensure(pos + 3u * S);
-    const uint32_t v0 = rd.peek_resident(pos);
-    const uint32_t f = (v0 & 1u) | ((rd.peek_resident(pos + S) & 1u) << 1) |
-                       ((rd.peek_resident(pos + 2u * S) & 1u) << 2) | ((rd.peek_resident(pos + 3u * S) & 1u) << 3);
-    int m = __ffs(~f) - 1;  // leading verbatim codes, 0..4
+    rd.ensure(pos + (kSkip - 1) * S);
+    uint32_t f = 0;
+#pragma unroll
+    for (int k = 0; k < kSkip; ++k) f |= rd.bit_resident(pos + (uint32_t)k * S) << k;
+    int m = __ffs(~f) - 1;  // leading verbatim codes, 0..kSkip
     if (m > i + 1) m = i + 1;
     if (m > 0) {
       pos += (uint32_t)m * S;
       i -= m;
       continue;
     }
+    const uint32_t v0 = rd.peek_resident(pos);
     const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4
     const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + p : 5u;
     const int run = (tz == 1u) ? 2 + (int)((v0 >> 2) & kmask) : 1;

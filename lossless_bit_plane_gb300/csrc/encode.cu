@@ -186,12 +186,10 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
   uint32_t nz = 0, zn = 0, adjz = 0, last = 0;                            // ZBX / ZVC
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Bw = 0, gdprev = 0;  // DBX
   uint32_t xprev = 0;
-  uint4 q = make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    if ((k & 3) == 0) q = stage_unit(rowbase, lane, (uint32_t)(k >> 2));
-    const uint32_t x = unit_word(q, k & 3);
-    uint32_t g = x ^ (x >> 1);
+  // word k of the block; the loop runs over 16-byte units (4 words each) so
+  // that the kernel's code stays small
+  auto step = [&](uint32_t x, uint32_t k) {
+    const uint32_t g = x ^ (x >> 1);
     ors |= x;
     c |= b & g;
     b |= a & g;
@@ -199,15 +197,15 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
     if (k) adj |= gprev & g;
     andx &= g;
     gprev = g;
-    uint32_t m = x ? 0xFFFFFFFFu : 0u;
+    const uint32_t m = x ? 0xFFFFFFFFu : 0u;
     nz |= m & (1u << k);
     zn |= ~g & m;  // some survivor has a 0 in the plane
     adjz |= last & g;
     last = x ? g : last;
     if (k) {
-      uint64_t d = (uint64_t)x - (uint64_t)xprev;
-      uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);  // hi: borrow mask
-      uint32_t gd = lo ^ __funnelshift_r(lo, hi, 1);
+      const uint64_t d = (uint64_t)x - (uint64_t)xprev;
+      const uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);  // hi: borrow mask
+      const uint32_t gd = lo ^ __funnelshift_r(lo, hi, 1);
       ord |= lo;
       Bw |= hi & (1u << (k - 1));
       cd |= bd & gd;
@@ -218,6 +216,21 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
       gdprev = gd;
     }
     xprev = x;
+  };
+  {
+    const uint4 q = stage_unit(rowbase, lane, 0);
+    step(q.x, 0);
+    step(q.y, 1);
+    step(q.z, 2);
+    step(q.w, 3);
+  }
+#pragma unroll 1
+  for (uint32_t u = 1; u < 8; ++u) {
+    const uint4 q = stage_unit(rowbase, lane, u);
+    step(q.x, 4 * u);
+    step(q.y, 4 * u + 1);
+    step(q.z, 4 * u + 2);
+    step(q.w, 4 * u + 3);
   }
   Sizes z;
   z.m0 = nz;
