@@ -55,6 +55,10 @@ cudaError_t device_info(DeviceInfo &out) {
         return e;
       if (d.enc_ctas_per_sm[w] < 1) return cudaErrorInvalidConfiguration;
     }
+    for (int w = 0; w < 2; ++w)
+      if ((e = cudaFuncSetAttribute(pz::walk_kernel_ptr(w == 1), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)pz::walk_smem_bytes())) != cudaSuccess)
+        return e;
     if (!g_encode_tiled) {
       void *fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -151,10 +155,17 @@ pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, voi
   a.status = d_status;
   a.num_chunks = (uint32_t)C;
   const bool w16 = (elem_width == 2);
+  DeviceInfo info;
+  if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
   void *args[1] = {&a};
+  const size_t G = pz::group_chunks();
+  const size_t groups = (C + G - 1) / G;
+  if (groups > 1 && cudaLaunchKernel(pz::size_sum_kernel_ptr(), dim3((unsigned)(groups - 1)), dim3(256), args, 0,
+                                     s) != cudaSuccess)
+    return PZ_ERR_CUDA;
   const size_t wt = (size_t)pz::walk_threads();
-  if (cudaLaunchKernel(pz::walk_kernel_ptr(w16), dim3((unsigned)((C + wt - 1) / wt)), dim3((unsigned)wt), args, 0,
-                       s) != cudaSuccess)
+  if (cudaLaunchKernel(pz::walk_kernel_ptr(w16), dim3((unsigned)((C + wt - 1) / wt)), dim3((unsigned)wt), args,
+                       pz::walk_smem_bytes(), s) != cudaSuccess)
     return PZ_ERR_CUDA;
   const size_t per = (size_t)pz::decode_chunks_per_cta();
   if (cudaLaunchKernel(pz::decode_kernel_ptr(w16), dim3((unsigned)((C + per - 1) / per)),

@@ -151,7 +151,7 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
     }
   }
   const bool dbx = (tag == kTagDBX);
-  const uint32_t p = (uint32_t)ceil_log2_int(W);
+  const uint32_t p = ceil_log2_u32((uint32_t)W);
   const uint32_t pmask = (1u << p) - 1u;
   // code length by class (leading zero bits, capped at 4), 7 bits each
   const uint32_t lens = (1u + (uint32_t)W) | ((2u + K) << 7) | (3u << 14) | ((5u + p) << 21);
@@ -301,166 +301,89 @@ struct WindowReader {  // straight from global memory (clamped to the input)
   __device__ __forceinline__ uint32_t peek(uint32_t pos) const { return win.peek32(base + pos); }
 };
 
-// Lane-private 512-byte ring in shared memory, filled ahead of the read
-// position with 16-byte cp.async copies (one commit group per copy), so a
-// lane streams its chunk without scattered global loads.
-constexpr uint32_t kRingUnits = 32;  // 16-byte units per ring
-constexpr uint32_t kRingAhead = 24;  // units kept in flight past the read unit
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_ahead() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(kRingAhead) : "memory");
-}
-
-struct RingReader {
-  uint32_t ring;       // shared address of the lane's ring
-  const uint8_t *g0;   // 16-byte aligned global address of unit 0
-  uint32_t nunits;     // units that hold chunk bytes
-  uint32_t fetched;    // units issued so far
-  uint32_t bit0;       // bit of unit 0 where the chunk starts
-  uint32_t limit;      // a peek at any q = bit0 + pos below this is resident
-
-  __device__ __forceinline__ void init(uint32_t ring_addr, const uint8_t *in, uint64_t off, uint32_t L) {
-    const uint64_t a0 = off & ~15ull;
-    ring = ring_addr;
-    g0 = in + a0;
-    bit0 = (uint32_t)(off - a0) * 8u;
-    nunits = (uint32_t)((off + L + 15 - a0) >> 4);
-    fetched = 0;
-    limit = 0;
-  }
-  __device__ __forceinline__ void refill(uint32_t q) {
-    const uint32_t need = ((q + 63) >> 7) + 1;  // units under a 64-bit window at q
-    const uint32_t lim = min(need + kRingAhead, nunits);
-    while (fetched < lim) {
-      cp_async16(ring + (fetched % kRingUnits) * 16u, g0 + 16ull * fetched);
-      ++fetched;
-    }
-    if (fetched == nunits) {
-      cp_async_wait_all();
-      limit = 0xFFFFFFFFu;
-    } else {
-      cp_async_wait_ahead();
-      limit = (fetched - kRingAhead) * 128u - 63u;  // q + 63 < resident units * 128
-    }
-  }
-  // 32 bits at chunk bit pos; the caller has ensured residency
-  __device__ __forceinline__ uint32_t peek_resident(uint32_t pos) const {
-    const uint32_t q = bit0 + pos;
-    const uint32_t w = q >> 5;
-    uint32_t lo, hi;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(lo) : "r"(ring + ((w & (kRingUnits * 4 - 1)) << 2)) : "memory");
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(hi) : "r"(ring + (((w + 1) & (kRingUnits * 4 - 1)) << 2)) : "memory");
-    return __funnelshift_r(lo, hi, q & 31u);
-  }
-  // the single bit at chunk bit pos (resident)
-  __device__ __forceinline__ uint32_t bit_resident(uint32_t pos) const {
-    const uint32_t q = bit0 + pos;
-    uint32_t w;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(ring + (((q >> 5) & (kRingUnits * 4 - 1)) << 2)) : "memory");
-    return (w >> (q & 31u)) & 1u;
-  }
-  // make every peek at or below pos resident
-  __device__ __forceinline__ void ensure(uint32_t pos) {
-    const uint32_t q = bit0 + pos;
-    if (q >= limit) refill(q);
-  }
-  __device__ __forceinline__ uint32_t peek(uint32_t pos) {
-    ensure(pos);
-    return peek_resident(pos);
-  }
-};
-
 struct WindowPeeker {  // adapts WindowReader to the ensure / peek_resident interface
   WindowReader r;
   __device__ __forceinline__ void ensure(uint32_t) const {}
   __device__ __forceinline__ uint32_t peek_resident(uint32_t pos) const { return r.peek(pos); }
   __device__ __forceinline__ uint32_t bit_resident(uint32_t pos) const { return r.peek(pos) & 1u; }
+  __device__ __forceinline__ void window_resident(uint32_t pos, uint32_t &v0, uint32_t &v1, uint32_t &v2) const {
+    v0 = r.peek(pos);
+    v1 = r.peek(pos + 32u);
+    v2 = r.peek(pos + 64u);
+  }
   __device__ __forceinline__ uint32_t peek(uint32_t pos) const { return r.peek(pos); }
 };
 
-// Advance pos over the plane codes of planes top..0 of width W. Each step
-// tests the flag bits of the next eight codes under the assumption that they
-// are verbatim (a verbatim code is 1 + W bits): a run of m leading verbatim
-// codes advances m planes at once; otherwise the code at pos is classified
-// by its leading zero bits (stream order, capped at 4): 01 run (2+K bits,
-// 2+field planes), 001 single zero (3), 0001x position code (5+p), 0000x
-// all-ones / pre-XOR-zero (5).
-template <typename Reader>
-__device__ __forceinline__ bool walk_planes(Reader &rd, uint32_t &pos, int top, int W, int K) {
-  constexpr int kSkip = 8;
-  const uint32_t p = (uint32_t)ceil_log2_int(W);
-  const uint32_t S = 1u + (uint32_t)W;
-  const uint32_t kmask = (1u << K) - 1u;
-  int i = top;
+// Walk one chunk: record each block's start bit (relative to the chunk)
+// through put_start(b, pos) and check that the chunk is exactly
+// ceil(bits/8) bytes with zero padding.
+//
+// The walk is one flat loop whose body is the same instruction stream for
+// every lane (selects, not branches), so that 32 lanes walking 32 chunks
+// stay converged however their blocks differ. An iteration either reads a
+// block header (tag; the mask of ZVC / ZBX; the base of DBX) and skips what
+// needs no parsing, or advances over plane codes: it tests the flag bits of
+// the next eight codes under the assumption that they are verbatim (1 + W
+// bits each) and skips the m leading verbatim ones, or, when the first code
+// is not verbatim, classifies it by its leading zero bits (stream order,
+// capped at 4): 01 run (2+K bits, 2+field planes), 001 single zero (3),
+// 0001x position code (5+p), 0000x all-ones / pre-XOR-zero (5).
+template <bool W16, typename Reader, typename Sink>
+__device__ __forceinline__ bool walk_chunk(Reader &rd, uint32_t L, uint32_t nblk, Sink put_start) {
+  constexpr uint32_t w = W16 ? 16u : 32u;   // bits per symbol = BX planes
+  constexpr uint32_t N = W16 ? 64u : 32u;   // symbols per block
+  constexpr uint32_t K = W16 ? 4u : 5u;     // run field
+  constexpr uint32_t kSkip = 8;
+  const uint32_t cap = 8u * L;
+  uint32_t pos = 0, b = 0;
+  int i = -1, top = 0;          // plane still to be walked (-1: next is a header)
+  uint32_t S = 2u, p = 0u;      // verbatim code length 1 + W, position field
   bool ok = true;
 #pragma unroll 1
-  while (i >= 0) {
-    rd.ensure(pos + (kSkip - 1) * S);
+  while (ok && (i >= 0 || b < nblk)) {
+    const bool hdr = i < 0;
+    rd.ensure(pos + (kSkip - 1) * S + 35u);
     uint32_t f = 0;
 #pragma unroll
-    for (int k = 0; k < kSkip; ++k) f |= rd.bit_resident(pos + (uint32_t)k * S) << k;
+    for (uint32_t k = 1; k < kSkip; ++k) f |= rd.bit_resident(pos + k * S) << k;
+    uint32_t v0, v1, v2;
+    rd.window_resident(pos, v0, v1, v2);
+    f |= v0 & 1u;
+    // header
+    const uint32_t tag = v0 & 7u;
+    const uint32_t n = __popc(__funnelshift_r(v0, v1, 3)) + (W16 ? __popc(__funnelshift_r(v1, v2, 3)) : 0u);
+    const bool masked = (tag == kTagZVC) || (tag == kTagZBX);
+    uint32_t hadv = 3u;
+    hadv += masked ? (W16 ? 64u : 32u) : 0u;
+    hadv += (tag == kTagZVC) ? n * w : 0u;
+    hadv += (tag == kTagDBX) ? w : 0u;
+    hadv += (tag == kTagRAW) ? 1024u : 0u;
+    const bool planes = (tag == kTagBX) || (tag == kTagDBX) || (tag == kTagZBX && n != 0);
+    const int htop = (tag == kTagDBX) ? (int)w : (int)w - 1;
+    const uint32_t hW = (tag == kTagDBX) ? N - 1u : (tag == kTagZBX) ? n : N;
+    // plane codes
     int m = __ffs(~f) - 1;  // leading verbatim codes, 0..kSkip
-    if (m > i + 1) m = i + 1;
-    if (m > 0) {
-      pos += (uint32_t)m * S;
-      i -= m;
-      continue;
-    }
-    const uint32_t v0 = rd.peek_resident(pos);
-    const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4
+    m = min(m, i + 1);
+    const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4 when not verbatim
     const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + p : 5u;
-    const int run = (tz == 1u) ? 2 + (int)((v0 >> 2) & kmask) : 1;
-    ok = ok && !(run > i + 1) && !(tz == 4u && (v0 & 16u) && i == top);
-    pos += len;
-    i -= run;
-  }
-  return ok;
-}
-
-// Record each block's start bit (relative to the chunk) and check that the
-// chunk is exactly ceil(bits/8) bytes with zero padding.
-template <bool W16, typename Reader>
-__device__ __forceinline__ bool walk_chunk(Reader &rd, uint32_t L, uint32_t nblk, uint16_t *starts) {
-  constexpr int w = W16 ? 16 : 32;
-  constexpr int N = W16 ? 64 : 32;
-  constexpr int K = W16 ? 4 : 5;
-  const uint32_t cap = 8u * L;
-  uint32_t pos = 0;
-#pragma unroll 1
-  for (uint32_t b = 0; b < nblk; ++b) {
-    starts[b] = (uint16_t)pos;
-    const uint32_t tag = rd.peek(pos) & 7u;
-    pos += 3;
-    if (tag > kTagRAW) return false;
-    if (tag == kTagRAW) {
-      pos += 1024;
-    } else if (tag == kTagZVC || tag == kTagZBX) {
-      uint32_t n = __popc(rd.peek(pos));
-      pos += 32;
-      if (W16) {
-        n += __popc(rd.peek(pos));
-        pos += 32;
-      }
-      if (tag == kTagZVC)
-        pos += n * w;
-      else if (n && !walk_planes(rd, pos, w - 1, (int)n, K))
-        return false;
+    const int run = (tz == 1u) ? 2 + (int)((v0 >> 2) & ((1u << K) - 1u)) : 1;
+    const bool pbad = (m == 0) && ((run > i + 1) || (tz == 4u && (v0 & 16u) && i == top));
+    if (hdr) {
+      put_start(b, pos);
+      ok = (tag <= kTagRAW) && pos <= cap;
+      pos += hadv;
+      i = planes ? htop : -1;
+      top = htop;
+      S = 1u + hW;
+      p = ceil_log2_u32(hW);
+      ++b;
     } else {
-      int top = w - 1, W = N;
-      if (tag == kTagDBX) {
-        pos += w;
-        top = w;
-        W = N - 1;
-      }
-      if (!walk_planes(rd, pos, top, W, K)) return false;
+      ok = !pbad;
+      pos += (m > 0) ? (uint32_t)m * S : len;
+      i -= (m > 0) ? m : run;
     }
-    if (pos > cap) return false;
   }
+  if (!ok || pos > cap) return false;
   if (cap - pos >= 8) return false;
   if (cap > pos && (rd.peek(pos) & ((1u << (cap - pos)) - 1u))) return false;
   return true;
@@ -468,44 +391,218 @@ __device__ __forceinline__ bool walk_chunk(Reader &rd, uint32_t L, uint32_t nblk
 
 // ---------------------------------------------------------------- kernels
 //
-// Two launches. The walk kernel runs one thread per chunk: it finds the
-// chunk's payload offset (sum of all earlier sizes) and, for a coded chunk,
-// every block's start bit, and leaves them in the first bytes of that
-// chunk's own output region: the offset (8 bytes) then the start bits of
-// blocks 1..n-1 (2 bytes each). The decode kernel runs one warp per chunk,
-// lane = block: each lane reads its start, the warp synchronises, and only
-// then are those bytes overwritten with decoded data. A final chunk too
-// short to hold that record (under 72 bytes) is located and walked by its
-// decode warp instead.
+// Up to three launches. The walk kernel runs one warp per 32 consecutive
+// chunks, lane = chunk: it finds each chunk's payload offset (2C plus the
+// sum of all earlier sizes) and, for a coded chunk, every block's start
+// bit, and leaves them in the first bytes of that chunk's own output region:
+// the offset (8 bytes) then the start bits of blocks 1..n-1 (2 bytes each).
+// The decode kernel runs one warp per chunk, lane = block: each lane reads
+// its start, the warp synchronises, and only then are those bytes
+// overwritten with decoded data. A final chunk too short to hold that record
+// (under 72 bytes) is located and walked by its decode warp instead.
+//
+// For the offsets, a first small kernel sums the sizes of each group of 2048
+// chunks (all groups but the last) and leaves the sum at byte 72 of the
+// group's first chunk region (a full 4 KB chunk, past its record); a walk
+// warp then adds at most one group sum per earlier group and the sizes of
+// at most 2047 chunks of its own group.
 
-constexpr int kWalkThreads = 64;
-constexpr int kRecordBytes = 72;  // 8-byte offset + 31 x 2-byte start bits + padding
+constexpr uint32_t kRecordBytes = 72;  // 8-byte offset + 31 x 2-byte start bits + padding
+constexpr uint32_t kGroupChunks = 2048;
+constexpr uint32_t kGroupSumAt = 72;   // byte of the group's first chunk region
+constexpr uint32_t kMbarPolls = 1u << 24;
 
-// Sum of the 16-bit sizes of chunks [0, first) by all threads of the block;
-// first must be a multiple of 8.
-__device__ __forceinline__ unsigned long long sum_sizes_before(const uint8_t *in, uint32_t first) {
-  unsigned long long part = 0;
-  const uint4 *h4 = reinterpret_cast<const uint4 *>(in);
-  for (uint32_t i = threadIdx.x; i < first / 8; i += blockDim.x) {
-    const uint4 v = __ldg(h4 + i);
-    part += (v.x & 0xFFFFu) + (v.x >> 16) + (v.y & 0xFFFFu) + (v.y >> 16) + (v.z & 0xFFFFu) + (v.z >> 16) +
-            (v.w & 0xFFFFu) + (v.w >> 16);
+__device__ __forceinline__ unsigned long long sum8_sizes(const uint4 v) {
+  return (unsigned long long)((v.x & 0xFFFFu) + (v.x >> 16) + (v.y & 0xFFFFu) + (v.y >> 16) + (v.z & 0xFFFFu) +
+                              (v.z >> 16) + (v.w & 0xFFFFu) + (v.w >> 16));
+}
+
+__global__ void __launch_bounds__(256) size_sum_kernel(DecodeArgs p) {
+  __shared__ unsigned long long red[8];
+  const uint32_t g = blockIdx.x;  // every chunk of the group exists
+  const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.in) + (uint64_t)g * (kGroupChunks / 8) + threadIdx.x);
+  const unsigned long long s = warp_sum_u64(sum8_sizes(v));
+  if (lane_id() == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    *reinterpret_cast<unsigned long long *>(p.out + (uint64_t)g * kGroupChunks * 4096u + kGroupSumAt) = t;
   }
-  return part;
+}
+
+// Sum of the sizes of chunks [0, first) (first a multiple of 32), by a warp.
+__device__ __forceinline__ unsigned long long sizes_before(const DecodeArgs &p, uint32_t first, uint32_t lane) {
+  const uint32_t g0 = first / kGroupChunks;
+  unsigned long long part = 0;
+  for (uint32_t g = lane; g < g0; g += 32)
+    part += *reinterpret_cast<const unsigned long long *>(p.out + (uint64_t)g * kGroupChunks * 4096u + kGroupSumAt);
+  const uint4 *h4 = reinterpret_cast<const uint4 *>(p.in);
+  for (uint32_t i = g0 * (kGroupChunks / 8) + lane; i < first / 8; i += 32) part += sum8_sizes(__ldg(h4 + i));
+  return warp_sum_u64(part);
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(mbar) : "memory");
+}
+// f with bit k replaced by bit 0 of v
+__device__ __forceinline__ uint32_t bit_insert(uint32_t f, uint32_t v, uint32_t k) {
+  uint32_t r;
+  asm("bfi.b32 %0, %1, %2, %3, 1;" : "=r"(r) : "r"(v), "r"(f), "r"(k));
+  return r;
+}
+
+// Walk kernel shape: warps of 32 chunks (lane = chunk); each lane reads its
+// chunk through a window of kWinUnits 16-byte units in shared memory.
+constexpr uint32_t kWalkWarps = 2;
+constexpr uint32_t kWinUnits = 48;
+constexpr uint32_t kWinWords = kWinUnits * 4;
+constexpr uint32_t kWalkSmem = kWalkWarps * 32 * kWinUnits * 16 + kWalkWarps * 8;
+
+// The warp's walk: lane = chunk. It is one loop that every lane runs until
+// the last lane is done (lanes that are done, or have nothing to walk, idle
+// through the selects), so that the warp stays converged: an iteration
+// either reads a block header (tag; the mask of ZVC / ZBX; the base of DBX)
+// and skips what needs no parsing, or advances over plane codes: it tests
+// the flag bits of the next eight codes under the assumption that they are
+// verbatim (1 + W bits each) and skips the m leading verbatim ones, or, when
+// the first code is not verbatim, classifies it by its leading zero bits
+// (stream order, capped at 4): 01 run (2+K bits, 2+field planes), 001
+// single zero (3), 0001x position code (5+p), 0000x all-ones / pre-XOR-zero
+// (5). A lane's window holds the units from the one under its position on;
+// when any lane's next iteration could read past its window, every walking
+// lane re-bases its window at its position with one bulk copy, and the warp
+// waits once for all of them. Records: the start bit of block b >= 1 goes to
+// rs[b - 1]. Returns false where the chunk is malformed.
+template <bool W16>
+__device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64_t off, uint32_t L, uint32_t nblk,
+                                          uint16_t *rs, const uint32_t *win, uint32_t mb, bool &timed_out) {
+  constexpr uint32_t w = W16 ? 16u : 32u;   // bits per symbol = BX planes
+  constexpr uint32_t N = W16 ? 64u : 32u;   // symbols per block
+  constexpr uint32_t K = W16 ? 4u : 5u;     // run field
+  constexpr uint32_t kSkip = 8;
+  constexpr uint32_t kAhead = (kSkip - 1) * (N + 1) + 128;  // bits an iteration may read past its position
+  const uint32_t lane = lane_id();
+  const uint64_t a0 = off & ~15ull;
+  const uint8_t *g0 = p.in + a0;
+  const uint32_t bit0 = (uint32_t)(off - a0) * 8u;
+  const uint32_t nunits = (uint32_t)((off + L + 15 - a0) >> 4);
+  const uint32_t cap = 8u * L;
+  const uint32_t winaddr = smem_u32(win);
+  uint32_t lim = 0;    // absolute bit at which the window ends
+  uint32_t wbase = 0;  // absolute bit where the window starts
+  uint32_t parity = 0;
+  uint32_t pos = 0, b = 0, S = 2u, pf = 0u;
+  int i = -1, top = 0;
+  bool ok = true;
+  bool run = walk;
+#pragma unroll 1
+  while (__any_sync(0xFFFFFFFFu, run)) {
+    const uint32_t qa = bit0 + min(pos, cap);
+    if (__any_sync(0xFFFFFFFFu, run && qa + kAhead >= lim)) {
+      fence_proxy_async_smem();  // this lane's reads of its window before the bulk write
+      if (run) {
+        const uint32_t u = qa >> 7;  // <= nunits
+        const uint32_t bytes = min(kWinUnits, nunits - u) * 16u;
+        if (bytes) {
+          mbar_expect_tx(mb, bytes);
+          bulk_load(winaddr, g0 + 16ull * u, bytes, mb);
+        }
+        wbase = u * 128u;
+        lim = wbase + kWinUnits * 128u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(mb);
+      const bool got = mbar_wait(mb, parity, kMbarPolls);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        mbar_wait(mb, parity, kMbarPolls);  // leave no copy in flight
+        timed_out = true;
+        return false;
+      }
+      parity ^= 1u;
+    }
+    // bit in the window; the clamp only binds for lanes that are done (a
+    // walking lane re-based its window above), and keeps every read inside
+    const uint32_t ql = min(qa - wbase, kWinUnits * 128u - kAhead);
+    uint32_t f = 0;
+#pragma unroll
+    for (uint32_t k = 1; k < kSkip; ++k) {
+      const uint32_t t = ql + k * S;
+      const uint32_t x = win[t >> 5];
+      f = bit_insert(f, __funnelshift_r(x, x, t), k);
+    }
+    const uint32_t wi = ql >> 5, sh = ql & 31u;
+    const uint32_t x0 = win[wi], x1 = win[wi + 1], x2 = win[wi + 2], x3 = win[wi + 3];
+    const uint32_t v0 = __funnelshift_r(x0, x1, sh), v1 = __funnelshift_r(x1, x2, sh), v2 = __funnelshift_r(x2, x3, sh);
+    f |= v0 & 1u;
+    // header
+    const uint32_t tag = v0 & 7u;
+    const uint32_t n = __popc(__funnelshift_r(v0, v1, 3)) + (W16 ? __popc(__funnelshift_r(v1, v2, 3)) : 0u);
+    const bool masked = (tag == kTagZVC) || (tag == kTagZBX);
+    uint32_t hadv = 3u;
+    hadv += masked ? (W16 ? 64u : 32u) : 0u;
+    hadv += (tag == kTagZVC) ? n * w : 0u;
+    hadv += (tag == kTagDBX) ? w : 0u;
+    hadv += (tag == kTagRAW) ? 1024u : 0u;
+    const bool planes = (tag == kTagBX) || (tag == kTagDBX) || (tag == kTagZBX && n != 0);
+    const int htop = (tag == kTagDBX) ? (int)w : (int)w - 1;
+    const uint32_t hW = (tag == kTagDBX) ? N - 1u : (tag == kTagZBX) ? n : N;
+    // plane codes
+    int m = __ffs(~f) - 1;  // leading verbatim codes, 0..kSkip
+    m = min(m, i + 1);
+    const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4 when not verbatim
+    const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
+    const int rl = (tz == 1u) ? 2 + (int)((v0 >> 2) & ((1u << K) - 1u)) : 1;
+    const bool pbad = (m == 0) && ((rl > i + 1) || (tz == 4u && (v0 & 16u) && i == top));
+    const bool hdr = i < 0;
+    if (run && hdr && b > 0) rs[b - 1] = (uint16_t)pos;
+    if (run) {
+      if (hdr) {
+        ok = (tag <= kTagRAW) && pos <= cap;
+        pos += hadv;
+        i = planes ? htop : -1;
+        top = htop;
+        S = 1u + hW;
+        pf = ceil_log2_u32(hW);
+        ++b;
+      } else {
+        ok = !pbad;
+        pos += (m > 0) ? (uint32_t)m * S : len;
+        i -= (m > 0) ? m : rl;
+      }
+      run = ok && (i >= 0 || b < nblk);
+    }
+  }
+  if (!walk) return true;
+  if (!ok || pos > cap || cap - pos >= 8) return false;
+  if (cap > pos) {  // the padding bits must be zero
+    const Window gw{reinterpret_cast<const uint32_t *>(p.in), (p.comp_bytes + 3) / 4};
+    if (gw.peek32(8ull * off + pos) & ((1u << (cap - pos)) - 1u)) return false;
+  }
+  return true;
 }
 
 template <bool W16>
-__global__ void __launch_bounds__(kWalkThreads)
+__global__ void __launch_bounds__(kWalkWarps * 32)
     walk_kernel(DecodeArgs p) {
-  __shared__ __align__(16) uint8_t rings[kWalkThreads][kRingUnits * 16];
-  __shared__ unsigned long long red[kWalkThreads / 32];
-  __shared__ uint32_t wsum[kWalkThreads / 32];
+  extern __shared__ __align__(128) uint8_t walk_smem[];
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t *win = reinterpret_cast<const uint32_t *>(walk_smem) + (warp * 32u + lane) * kWinWords;
+  const uint32_t mb = smem_u32(walk_smem + kWalkWarps * 32 * kWinUnits * 16) + warp * 8u;
   const uint32_t C = p.num_chunks;
-  const uint32_t first = blockIdx.x * kWalkThreads;
-  unsigned long long part = warp_sum_u64(sum_sizes_before(p.in, first));
-  const uint32_t c = first + threadIdx.x;
+  const uint32_t first = (blockIdx.x * kWalkWarps + warp) * 32u;
+  if (first >= C) return;
+  const uint32_t c = first + lane;
   const bool valid = c < C;
+  const unsigned long long before = sizes_before(p, first, lane);
   const uint32_t L = valid ? __ldg(reinterpret_cast<const uint16_t *>(p.in) + c) : 0u;
   uint32_t incl = L;
 #pragma unroll
@@ -513,36 +610,28 @@ __global__ void __launch_bounds__(kWalkThreads)
     const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= (uint32_t)o) incl += v;
   }
-  if (lane == 0) red[warp] = part;
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  if (!valid) return;
-  unsigned long long base = 0;
-  for (int w = 0; w < kWalkThreads / 32; ++w) base += red[w];
-  for (uint32_t w = 0; w < warp; ++w) base += wsum[w];
-  const uint64_t off = 2ull * C + base + (incl - L);
-  const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
-  if (L == 0 || L > raw_len || off + L > p.comp_bytes) {
-    atomicMax(p.status, kErrCorrupt);
-    return;
-  }
-  if (raw_len < (uint32_t)kRecordBytes) return;  // the decode warp handles it
+  const uint64_t off = 2ull * C + before + (incl - L);
+  const uint32_t raw_len = valid ? (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u) : 0u;
+  const bool bad = valid && (L == 0 || L > raw_len || off + L > p.comp_bytes);
+  if (bad) atomicMax(p.status, kErrCorrupt);
   uint8_t *rec = p.out + (uint64_t)c * 4096u;
-  *reinterpret_cast<unsigned long long *>(rec) = off;
-  if (L == raw_len) return;  // raw chunk: the offset is all the decoder needs
-  uint16_t starts[32];
-  RingReader rd;
-  rd.init(smem_u32(rings[threadIdx.x]), p.in, off, L);
-  const uint32_t nblk = (raw_len + 127u) >> 7;
-  const bool ok = walk_chunk<W16>(rd, L, nblk, starts);
-  cp_async_wait_all();  // no copy may be in flight when the thread exits
-  if (!ok) {
-    atomicMax(p.status, kErrCorrupt);
-    return;
+  const bool has_rec = valid && !bad && raw_len >= kRecordBytes;
+  if (has_rec) *reinterpret_cast<unsigned long long *>(rec) = off;
+  const bool walk = has_rec && L < raw_len;  // a raw chunk needs only its offset
+  if (!__any_sync(0xFFFFFFFFu, walk)) return;
+  if (lane == 0) {
+    mbar_init(mb, 1);
+    fence_mbar_init();
   }
-  uint16_t *rs = reinterpret_cast<uint16_t *>(rec + 8);
-#pragma unroll 1
-  for (uint32_t b = 1; b < nblk; ++b) rs[b - 1] = starts[b];
+  __syncwarp();
+  bool timed_out = false;
+  const bool ok = walk_warp<W16>(p, walk, off, L, (raw_len + 127u) >> 7, reinterpret_cast<uint16_t *>(rec + 8), win,
+                                 mb, timed_out);
+  if (timed_out) {
+    if (lane == 0) atomicMax(p.status, kErrTimeout);
+  } else if (!ok) {
+    atomicMax(p.status, kErrCorrupt);
+  }
 }
 
 // Byte offset of 16-byte unit u of row r in a 128-byte-swizzled 4 KB tile.
@@ -586,7 +675,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
     if (L < raw_len) {
       if (lane == 0) {
         WindowPeeker rd{WindowReader{win, 8ull * off}};
-        ok = walk_chunk<W16>(rd, L, nblk, tail_starts[warp]);
+        uint16_t *ts = tail_starts[warp];
+        ok = walk_chunk<W16>(rd, L, nblk, [ts](uint32_t b, uint32_t pos) { ts[b] = (uint16_t)pos; });
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
       if (!ok) {
@@ -670,7 +760,10 @@ template __global__ void walk_kernel<true>(DecodeArgs);
 template __global__ void decode_kernel<false>(DecodeArgs);
 template __global__ void decode_kernel<true>(DecodeArgs);
 
-int walk_threads() { return kWalkThreads; }
+int walk_threads() { return kWalkWarps * 32; }
+size_t walk_smem_bytes() { return kWalkSmem; }
+uint32_t group_chunks() { return kGroupChunks; }
+const void *size_sum_kernel_ptr() { return reinterpret_cast<const void *>(&size_sum_kernel); }
 int decode_threads() { return kDecWarps * 32; }
 int decode_chunks_per_cta() { return kDecWarps; }
 const void *walk_kernel_ptr(bool w16) {

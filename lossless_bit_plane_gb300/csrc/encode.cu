@@ -248,7 +248,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
     zbx = make_plan(0, 0, 0, 0, 0, 1, 0);
     z.s[kTagZBX] = 32;
   } else {
-    const int pn = ceil_log2_int(n);
+    const int pn = (int)ceil_log2_u32((uint32_t)n);
     zbx = make_plan(a, ~zn & a, PX, a & ~b, b & ~c & adjz, n, pn);
     z.s[kTagZBX] = 32 + run_cost((uint32_t)~a, 5) + plan_cost(zbx, n, pn);
   }
@@ -354,7 +354,7 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane) {
   } else {
     const uint32_t adjz16 = lo(adjz) | hi(adjz) | (lo(last) & hi(fst));
     const uint32_t A = ~(lo(zn) | hi(zn)) & a16;
-    const int pn = ceil_log2_int(n);
+    const int pn = (int)ceil_log2_u32((uint32_t)n);
     zbx = make_plan(a16, A, PX16, a16 & ~b16, b16 & ~c16 & adjz16, n, pn);
     z.s[kTagZBX] = 64 + run_cost(Z16, 4) + plan_cost(zbx, n, pn);
   }
@@ -556,7 +556,7 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t nz,
   transpose32(T);
 #pragma unroll
   for (int i = 0; i < 32; ++i) sts32(plane_row(rowbase, lane, i), T[i]);
-  emit_plane_codes<false>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv, pl);
+  emit_plane_codes<false>(bw, rowbase, lane, top, W, (int)ceil_log2_u32((uint32_t)W), tag == kTagDBX, topv, pl);
 }
 
 // BF16 emit of the chosen candidate. sp: split-packed symbols (word j =
@@ -629,7 +629,7 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t mlo
   transpose32(T);
 #pragma unroll
   for (int i = 0; i < 32; ++i) sts32(plane_row(rowbase, lane, i), T[i]);
-  emit_plane_codes<true>(bw, rowbase, lane, top, W, ceil_log2_int(W), tag == kTagDBX, topv, pl);
+  emit_plane_codes<true>(bw, rowbase, lane, top, W, (int)ceil_log2_u32((uint32_t)W), tag == kTagDBX, topv, pl);
 }
 
 // --------------------------------------------------------------- look-back

@@ -14,6 +14,8 @@ namespace pz {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+// ceil(log2(v)) for v >= 1 (0 for v <= 1), without a loop
+__device__ __forceinline__ uint32_t ceil_log2_u32(uint32_t v) { return v <= 1u ? 0u : 32u - (uint32_t)__clz(v - 1u); }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;

@@ -34,7 +34,10 @@ int encode_warps();
 const void *encode_kernel_ptr(bool w16);
 
 int walk_threads();
+size_t walk_smem_bytes();
 const void *walk_kernel_ptr(bool w16);
+uint32_t group_chunks();              // chunks per size-sum group
+const void *size_sum_kernel_ptr();    // 256 threads, one block per group but the last
 int decode_threads();
 int decode_chunks_per_cta();
 const void *decode_kernel_ptr(bool w16);
