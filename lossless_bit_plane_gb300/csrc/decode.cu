@@ -562,24 +562,22 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
     const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
     const int rl = (tz == 1u) ? 2 + (int)((v0 >> 2) & ((1u << K) - 1u)) : 1;
     const bool pbad = (m == 0) && ((rl > i + 1) || (tz == 4u && (v0 & 16u) && i == top));
+    // next state, by selects: a header iteration, a plane iteration, or
+    // none (the lane is done)
     const bool hdr = i < 0;
-    if (run && hdr && b > 0) rs[b - 1] = (uint16_t)pos;
-    if (run) {
-      if (hdr) {
-        ok = (tag <= kTagRAW) && pos <= cap;
-        pos += hadv;
-        i = planes ? htop : -1;
-        top = htop;
-        S = 1u + hW;
-        pf = ceil_log2_u32(hW);
-        ++b;
-      } else {
-        ok = !pbad;
-        pos += (m > 0) ? (uint32_t)m * S : len;
-        i -= (m > 0) ? m : rl;
-      }
-      run = ok && (i >= 0 || b < nblk);
-    }
+    const bool hrun = run && hdr, prun = run && !hdr;
+    if (hrun && b > 0) rs[b - 1] = (uint16_t)pos;
+    const bool verb = m > 0;
+    const uint32_t padv = verb ? (uint32_t)m * S : len;
+    const int pdec = verb ? m : rl;
+    ok = hrun ? ((tag <= kTagRAW) && pos <= cap) : prun ? !pbad : ok;
+    pos += hrun ? hadv : prun ? padv : 0u;
+    i = hrun ? (planes ? htop : -1) : prun ? i - pdec : i;
+    top = hrun ? htop : top;
+    S = hrun ? 1u + hW : S;
+    pf = hrun ? ceil_log2_u32(hW) : pf;
+    b += hrun ? 1u : 0u;
+    run = run && ok && (i >= 0 || b < nblk);
   }
   if (!walk) return true;
   if (!ok || pos > cap || cap - pos >= 8) return false;
