@@ -276,24 +276,18 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane) {
            gd0 = 0;
   const uint32_t s31lo = stage_unit(rowbase, lane, 3).w & 0xFFFF0000u;  // symbol 31 in the high half
   uint32_t xprev = 0;
-  uint4 qa = make_uint4(0, 0, 0, 0), qb = make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if ((j & 7) == 0) {
-      qa = stage_unit(rowbase, lane, (uint32_t)(j >> 3));
-      qb = stage_unit(rowbase, lane, 4u + (uint32_t)(j >> 3));
-    }
-    const uint32_t x = prmt(unit_word(qa, (j >> 1) & 3), unit_word(qb, (j >> 1) & 3), (j & 1) ? 0x7632u : 0x5410u);
-    uint32_t g = x ^ ((x >> 1) & 0x7FFF7FFFu);
+  // split-packed word j >= 1 (symbols j and j+32); the loop below runs over
+  // half 16-byte units (4 words each) so that the kernel's code stays small
+  auto step = [&](uint32_t x, uint32_t j) {
+    const uint32_t g = x ^ ((x >> 1) & 0x7FFF7FFFu);
     ors |= x;
     c |= b & g;
     b |= a & g;
     a |= g;
-    if (j) adj |= gprev & g;
-    else g0 = g;
+    adj |= gprev & g;
     andx &= g;
     gprev = g;
-    uint32_t m = halfmask_nonzero(x);
+    const uint32_t m = halfmask_nonzero(x);
     mlo |= (m & 1u) << j;
     mhi |= (m >> 31) << j;
     zn |= ~g & m;
@@ -301,29 +295,63 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane) {
     last = (g & m) | (last & ~m);
     fst |= g & ~seen;
     seen |= m;
-    // DBX: lo half d_j = s_j - s_{j-1} (j >= 1), hi half d_{j+32} = s_{j+32} - s_{j+31}
+    // DBX: lo half d_j = s_j - s_{j-1}, hi half d_{j+32} = s_{j+32} - s_{j+31}
     uint32_t bo;
-    uint32_t d = sub16x2(x, j ? xprev : s31lo, bo);
-    if (j == 0) {
-      d &= 0xFFFF0000u;
-      bo &= 0x80000000u;
-    }
-    uint32_t gd = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
+    const uint32_t d = sub16x2(x, xprev, bo);
+    const uint32_t gd = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
     ord |= d;
     cd |= bd & gd;
     bd |= ad & gd;
     ad |= gd;
-    andd &= (j == 0) ? (gd | 0x0000FFFFu) : gd;
-    if (j) adjd |= gdprev & gd;
-    else gd0 = gd;
+    andd &= gd;
+    adjd |= gdprev & gd;
     gdprev = gd;
-    if (j == 0) {
-      Blo |= bo & 0x80000000u;  // d_32's borrow -> plane position 31
-    } else {
-      Blo |= ((bo >> 15) & 1u) << (j - 1);  // d_j -> position j-1
-      Bhi |= (bo >> 31) << (j - 1);         // d_{j+32} -> position j+31
-    }
+    Blo |= ((bo >> 15) & 1u) << (j - 1);  // d_j -> position j-1
+    Bhi |= (bo >> 31) << (j - 1);         // d_{j+32} -> position j+31
     xprev = x;
+  };
+  {
+    const uint4 qa = stage_unit(rowbase, lane, 0), qb = stage_unit(rowbase, lane, 4);
+    // word 0: no delta for symbol 0 (the DBX base); d_32 = s_32 - s_31
+    const uint32_t x = prmt(qa.x, qb.x, 0x5410u);
+    const uint32_t g = x ^ ((x >> 1) & 0x7FFF7FFFu);
+    ors = x;
+    a = g;
+    g0 = g;
+    andx = g;
+    gprev = g;
+    const uint32_t m = halfmask_nonzero(x);
+    mlo = m & 1u;
+    mhi = m >> 31;
+    zn = ~g & m;
+    last = g & m;
+    fst = g;
+    seen = m;
+    uint32_t bo;
+    uint32_t d = sub16x2(x, s31lo, bo);
+    d &= 0xFFFF0000u;
+    bo &= 0x80000000u;
+    const uint32_t gd = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
+    ord = d;
+    ad = gd;
+    andd = gd | 0x0000FFFFu;
+    gd0 = gd;
+    gdprev = gd;
+    Blo = bo;  // d_32's borrow -> plane position 31
+    xprev = x;
+    step(prmt(qa.x, qb.x, 0x7632u), 1);
+    step(prmt(qa.y, qb.y, 0x5410u), 2);
+    step(prmt(qa.y, qb.y, 0x7632u), 3);
+  }
+#pragma unroll 1
+  for (uint32_t h = 1; h < 8; ++h) {
+    const uint4 qa = stage_unit(rowbase, lane, h >> 1), qb = stage_unit(rowbase, lane, 4u + (h >> 1));
+    const bool hi = (h & 1u) != 0;
+    const uint32_t a0 = hi ? qa.z : qa.x, a1 = hi ? qa.w : qa.y, b0 = hi ? qb.z : qb.x, b1 = hi ? qb.w : qb.y;
+    step(prmt(a0, b0, 0x5410u), 4u * h);
+    step(prmt(a0, b0, 0x7632u), 4u * h + 1u);
+    step(prmt(a1, b1, 0x5410u), 4u * h + 2u);
+    step(prmt(a1, b1, 0x7632u), 4u * h + 3u);
   }
   // combine the two halves (symbols 0..31 and 32..63) into 16-plane masks
   auto lo = [](uint32_t v) { return v & 0xFFFFu; };
