@@ -24,6 +24,7 @@ _LIB = _HERE / "libpzoracle.so"
 OK, ERR_ARG, ERR_CAPACITY, ERR_CORRUPT = 0, 1, 2, 3
 TAG_ZVC, TAG_DBX, TAG_BX, TAG_ZBX, TAG_RAW = 0, 1, 2, 3, 4
 TAG_NAMES = ("ZVC", "DBX", "BX", "ZBX", "RAW")
+CAND_ALL = 0x1F  # candidate mask: bit t = tag t; the raw block is always allowed
 
 _lib = None
 
@@ -59,6 +60,10 @@ def lib():
         L.pzo_encode_candidate.restype = ctypes.c_int
         L.pzo_analyze.argtypes = [u8p, sz, ctypes.c_int, u8p, u8p, u8p]
         L.pzo_analyze.restype = ctypes.c_int
+        L.pzo_compress_candidates.argtypes = [u8p, sz, ctypes.c_int, ctypes.c_uint, u8p, sz, ctypes.POINTER(sz)]
+        L.pzo_compress_candidates.restype = ctypes.c_int
+        L.pzo_analyze_candidates.argtypes = [u8p, sz, ctypes.c_int, ctypes.c_uint, u8p, u8p, u8p]
+        L.pzo_analyze_candidates.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -75,13 +80,15 @@ def max_stream_bytes(nbytes: int) -> int:
     return int(lib().pzo_max_stream_bytes(nbytes))
 
 
-def compress(data, elem_width: int) -> bytes:
-    """Compress a byte buffer (bytes or numpy array); returns the stream."""
+def compress(data, elem_width: int, candidates: int = CAND_ALL) -> bytes:
+    """Compress a byte buffer (bytes or numpy array); returns the stream.
+    ``candidates`` restricts block selection (bit t = tag t; raw always)."""
     src = _u8(data)
     cap = max_stream_bytes(src.size)
     out = np.zeros(max(cap, 1), dtype=np.uint8)
     total = ctypes.c_size_t(0)
-    rc = lib().pzo_compress(_ptr(src), src.size, elem_width, _ptr(out), cap, ctypes.byref(total))
+    rc = lib().pzo_compress_candidates(_ptr(src), src.size, elem_width, candidates, _ptr(out), cap,
+                                       ctypes.byref(total))
     if rc != OK:
         raise RuntimeError(f"pzo_compress failed with status {rc}")
     return out[: total.value].tobytes()
@@ -122,7 +129,7 @@ def encode_candidate(block, elem_width: int, tag: int) -> tuple[int, bytes]:
     return n, buf[: (n + 7) // 8].tobytes()
 
 
-def analyze(data, elem_width: int):
+def analyze(data, elem_width: int, candidates: int = CAND_ALL):
     """Per-block tags and bit counts and per-chunk L for a whole buffer."""
     src = _u8(data)
     nb = (src.size + 127) // 128
@@ -130,6 +137,7 @@ def analyze(data, elem_width: int):
     tags = np.zeros(max(nc * 32, 1), dtype=np.uint8)
     bits = np.zeros(max(nc * 32, 1), dtype=np.uint16)
     lens = np.zeros(max(nc, 1), dtype=np.uint16)
-    rc = lib().pzo_analyze(_ptr(src), src.size, elem_width, _ptr(tags), _ptr(bits), _ptr(lens))
+    rc = lib().pzo_analyze_candidates(_ptr(src), src.size, elem_width, candidates, _ptr(tags), _ptr(bits),
+                                      _ptr(lens))
     assert rc == OK
     return tags[:nb], bits[:nb], lens[:nc]

@@ -452,11 +452,14 @@ static void candidate_bits_by_model(const uint8_t *block, geometry g, int out[5]
   out[PZO_TAG_RAW] = BLOCK_BYTES * 8;
 }
 
-/* The block keeps the smallest candidate; ties go to the lowest tag (R12). */
-static int select_tag(const int bits[5]) {
-  int best = 0;
-  for (int t = 1; t < 5; t++)
-    if (bits[t] < bits[best]) best = t;
+/* The block keeps the smallest candidate; ties go to the lowest tag (R12).
+ * Only the candidates in the mask `allowed` (bit t = tag t) are considered;
+ * the raw block is always allowed, so a choice always exists. */
+static int select_tag(const int bits[5], unsigned allowed) {
+  allowed |= 1u << PZO_TAG_RAW;
+  int best = PZO_TAG_RAW;
+  for (int t = 0; t < 5; t++)
+    if (((allowed >> t) & 1u) && (bits[t] < bits[best] || (bits[t] == bits[best] && t < best))) best = t;
   return best;
 }
 
@@ -530,7 +533,7 @@ size_t pzo_max_stream_bytes(size_t nbytes) { return 2 * num_chunks(nbytes) + nby
 
 /* Encode one chunk of raw_len bytes into `payload`; returns its length L
  * and fills per-block tags/bits when asked. */
-static size_t encode_chunk(const uint8_t *src, size_t raw_len, geometry g, uint8_t *payload,
+static size_t encode_chunk(const uint8_t *src, size_t raw_len, geometry g, unsigned allowed, uint8_t *payload,
                            uint8_t *tags, uint16_t *bits) {
   uint8_t coded[CHUNK_BYTES + 64];
   memset(coded, 0, sizeof(coded));
@@ -545,7 +548,7 @@ static size_t encode_chunk(const uint8_t *src, size_t raw_len, geometry g, uint8
     memcpy(block, src + b * BLOCK_BYTES, take);
     int cand[5];
     candidate_bits_by_encoding(block, g, cand);
-    int tag = select_tag(cand);
+    int tag = select_tag(cand, allowed);
     size_t start = w.pos;
     put_field(&w, (uint64_t)tag, 3);
     block_to_symbols(block, g, s);
@@ -566,6 +569,11 @@ static size_t encode_chunk(const uint8_t *src, size_t raw_len, geometry g, uint8
 
 int pzo_compress(const uint8_t *in, size_t nbytes, int elem_width, uint8_t *out, size_t cap,
                  size_t *total) {
+  return pzo_compress_candidates(in, nbytes, elem_width, PZO_CAND_ALL, out, cap, total);
+}
+
+int pzo_compress_candidates(const uint8_t *in, size_t nbytes, int elem_width, unsigned candidates,
+                            uint8_t *out, size_t cap, size_t *total) {
   if (elem_width <= 0 || (!in && nbytes) || !total) return PZO_ERR_ARG;
   size_t C = num_chunks(nbytes);
   if (cap < pzo_max_stream_bytes(nbytes)) return PZO_ERR_CAPACITY;
@@ -575,7 +583,7 @@ int pzo_compress(const uint8_t *in, size_t nbytes, int elem_width, uint8_t *out,
   for (size_t c = 0; c < C; c++) {
     size_t raw_len = nbytes - c * CHUNK_BYTES;
     if (raw_len > CHUNK_BYTES) raw_len = CHUNK_BYTES;
-    size_t L = encode_chunk(in + c * CHUNK_BYTES, raw_len, g, out + pos, NULL, NULL);
+    size_t L = encode_chunk(in + c * CHUNK_BYTES, raw_len, g, candidates, out + pos, NULL, NULL);
     out[2 * c] = (uint8_t)(L & 0xFF);
     out[2 * c + 1] = (uint8_t)(L >> 8);
     pos += L;
@@ -628,7 +636,7 @@ int pzo_block_candidates(const uint8_t block[128], int elem_width, int enc_bits[
   candidate_bits_by_encoding(block, g, e);
   if (enc_bits) memcpy(enc_bits, e, sizeof(e));
   if (model_bits) candidate_bits_by_model(block, g, model_bits);
-  if (tag) *tag = select_tag(e);
+  if (tag) *tag = select_tag(e, PZO_CAND_ALL);
   return PZO_OK;
 }
 
@@ -645,6 +653,11 @@ int pzo_encode_candidate(const uint8_t block[128], int elem_width, int tag, uint
 
 int pzo_analyze(const uint8_t *in, size_t nbytes, int elem_width, uint8_t *tags, uint16_t *bits,
                 uint16_t *lens) {
+  return pzo_analyze_candidates(in, nbytes, elem_width, PZO_CAND_ALL, tags, bits, lens);
+}
+
+int pzo_analyze_candidates(const uint8_t *in, size_t nbytes, int elem_width, unsigned candidates,
+                           uint8_t *tags, uint16_t *bits, uint16_t *lens) {
   if (elem_width <= 0 || (!in && nbytes)) return PZO_ERR_ARG;
   geometry g = geometry_for(elem_width);
   size_t C = num_chunks(nbytes);
@@ -652,7 +665,7 @@ int pzo_analyze(const uint8_t *in, size_t nbytes, int elem_width, uint8_t *tags,
   for (size_t c = 0; c < C; c++) {
     size_t raw_len = nbytes - c * CHUNK_BYTES;
     if (raw_len > CHUNK_BYTES) raw_len = CHUNK_BYTES;
-    size_t L = encode_chunk(in + c * CHUNK_BYTES, raw_len, g, payload,
+    size_t L = encode_chunk(in + c * CHUNK_BYTES, raw_len, g, candidates, payload,
                             tags ? tags + c * BLOCKS_PER_CHUNK : NULL,
                             bits ? bits + c * BLOCKS_PER_CHUNK : NULL);
     if (lens) lens[c] = (uint16_t)L;

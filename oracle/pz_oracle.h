@@ -44,6 +44,9 @@ enum {
 
 enum { PZO_TAG_ZVC = 0, PZO_TAG_DBX = 1, PZO_TAG_BX = 2, PZO_TAG_ZBX = 3, PZO_TAG_RAW = 4 };
 
+/* Candidate masks (bit t = tag t). The raw block is always a candidate. */
+#define PZO_CAND_ALL 0x1Fu
+
 /* Largest possible stream for nbytes of input: 2 bytes of header per chunk
  * plus every chunk stored raw. */
 size_t pzo_max_stream_bytes(size_t nbytes);
@@ -53,6 +56,14 @@ size_t pzo_max_stream_bytes(size_t nbytes);
  * other positive width selects 32-bit symbols. */
 int pzo_compress(const uint8_t *in, size_t nbytes, int elem_width,
                  uint8_t *out, size_t cap, size_t *total);
+
+/* The same stream format with block selection restricted to the candidates
+ * in `candidates` (bit t = tag t; raw is always allowed): the smallest
+ * allowed candidate is kept, ties to the lowest tag. PZO_CAND_ALL gives
+ * pzo_compress. This reproduces the paper's single-encoding comparisons
+ * (Section IV-B, Fig. 3: ZVC only, BPC = DBX on every block, ...). */
+int pzo_compress_candidates(const uint8_t *in, size_t nbytes, int elem_width, unsigned candidates,
+                            uint8_t *out, size_t cap, size_t *total);
 
 /* Decompress a stream of comp_bytes (>= the stream's own length) into
  * nbytes at `out`. Returns PZO_ERR_CORRUPT on any malformed field. */
@@ -78,6 +89,10 @@ int pzo_encode_candidate(const uint8_t block[128], int elem_width, int tag,
  * ceil(nbytes/128) and ceil(nbytes/4096) entries. */
 int pzo_analyze(const uint8_t *in, size_t nbytes, int elem_width,
                 uint8_t *tags, uint16_t *bits, uint16_t *lens);
+
+/* pzo_analyze with block selection restricted as in pzo_compress_candidates. */
+int pzo_analyze_candidates(const uint8_t *in, size_t nbytes, int elem_width, unsigned candidates,
+                           uint8_t *tags, uint16_t *bits, uint16_t *lens);
 
 #ifdef __cplusplus
 }
