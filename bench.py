@@ -330,6 +330,7 @@ def run_ours(args, rank: int, world: int, local: int):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, segs, d_out, d_back, d_tot, d_st, totals_host, dev, stream, world, dist)
+    sizes = run_sizes(args, segs, d_in, totals_host, dev, stream)
 
     per_seg = []
     for i, t in enumerate(segs):
@@ -371,12 +372,83 @@ def run_ours(args, rank: int, world: int, local: int):
         "clocks": clk,
         "segments": per_seg,
         "eq2": eq2(raw / comp, raw / (tc_ms * 1e-3) / 1e9),
+        "size_only": sizes["size_only"],
+        "ablation": sizes["ablation"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def run_sizes(args, segs, d_in, totals_host, dev, stream):
+    """Outside the headline's timed region: the sizes-only entry point
+    (pz_compressed_size) timed over the same segments, every chunk and every
+    fourth chunk (the paper's sampling of large tensors), and the codec
+    ablation of the paper's Fig. 3 -- the exact ratio of each single-encoding
+    candidate mask and of BF16 coded with 32-bit symbols, over the sweep's
+    activation segments (the uniform-random segment is left out)."""
+    import torch
+
+    from lossless_bit_plane_gb300 import _lib
+
+    sh = stream.cuda_stream
+    n = len(segs)
+    d_tot = torch.zeros(n, dtype=torch.int64, device=dev)
+
+    def sizes_all(stride, mask=_lib.PZ_CAND_ALL, width=None):
+        for i, t in enumerate(segs):
+            rc = _lib.pz_compressed_size(d_in[i].data_ptr(), t.nbytes, width or t.elem_width, mask, stride, 0,
+                                         d_tot[i:i + 1].data_ptr(), sh)
+            assert rc == 0, rc
+
+    def timed(stride, reps):
+        for _ in range(2):
+            sizes_all(stride)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            sizes_all(stride)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    raw = sum(t.nbytes for t in segs)
+    reps = max(1, min(args.steps, 5))
+    ms1 = timed(1, reps)
+    tot1 = d_tot.cpu().tolist()
+    assert tot1 == totals_host, "sizes-only totals differ from the compressed streams"
+    ms4 = timed(4, reps)
+    tot4 = d_tot.cpu().tolist()
+    sampled_raw = sum(min(t.nbytes - 4096 * c, 4096) for t in segs for c in range(0, (t.nbytes + 4095) // 4096, 4))
+    size_only = {"unit": "GB/s", "gbs": raw / (ms1 * 1e-3) / 1e9, "sampled_every_4th_gbs": raw / (ms4 * 1e-3) / 1e9,
+                 "ratio": raw / sum(tot1), "sampled_ratio_estimate": sampled_raw / sum(tot4),
+                 "launches_per_pass": n}
+
+    groups = {"fp32": [i for i, t in enumerate(segs) if t.elem_width == 4 and not t.name.startswith("random")],
+              "bf16": [i for i, t in enumerate(segs) if t.elem_width == 2]}
+    masks = {"planezip": _lib.PZ_CAND_ALL, "zvc": _lib.PZ_CAND_ZVC, "bpc_dbx": _lib.PZ_CAND_DBX,
+             "bx": _lib.PZ_CAND_BX, "zbx": _lib.PZ_CAND_ZBX}
+    ablation = {"source": "Section V-A, Fig. 3 (single encodings vs the per-block choice; BF16 with 32-bit "
+                          "symbols); ratios over the sweep's activation segments, uniform-random excluded"}
+    for g, idx in groups.items():
+        if not idx:
+            continue
+        graw = sum(segs[i].nbytes for i in idx)
+        row = {}
+        for name, m in masks.items():
+            sizes_all(1, m)
+            tot = d_tot.cpu().tolist()
+            row[name] = round(graw / sum(tot[i] for i in idx), 4)
+        row["best_single"] = max(row[k] for k in ("zvc", "bpc_dbx", "bx", "zbx"))
+        if g == "bf16":
+            sizes_all(1, _lib.PZ_CAND_ALL, width=4)
+            tot = d_tot.cpu().tolist()
+            row["planezip_with_32bit_symbols"] = round(graw / sum(tot[i] for i in idx), 4)
+        ablation[g] = row
+    return {"size_only": size_only, "ablation": ablation}
 
 
 def run_e2e(args, segs, d_out, d_back, d_tot, d_st, totals_host, dev, stream, world, dist):

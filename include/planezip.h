@@ -105,6 +105,59 @@ pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width,
                         void *d_out, size_t nbytes, int *d_status,
                         pz_stream_t stream);
 
+/* Candidate masks for block selection: bit t allows the encoding with tag t
+ * (Section III-A "Codec": ZVC 0, DBX 1, BX 2, ZBX 3, raw 4). The raw block is
+ * always allowed, so every mask gives a valid stream in the same format. */
+#define PZ_CAND_ZVC 0x01u
+#define PZ_CAND_DBX 0x02u
+#define PZ_CAND_BX 0x04u
+#define PZ_CAND_ZBX 0x08u
+#define PZ_CAND_RAW 0x10u
+#define PZ_CAND_ALL 0x1Fu
+
+/* pz_compress with block selection restricted to `candidates` (a mask of
+ * PZ_CAND_* bits; PZ_CAND_RAW is implied): each block keeps the smallest
+ * ALLOWED candidate, ties to the lowest tag; chunks that would grow are
+ * still stored raw. PZ_CAND_ALL is pz_compress. The stream decodes with
+ * pz_decompress like any other.
+ * Source: Section V-A "Compression Ratio" and Fig. 3, which compare PlaneZip
+ * with single encodings applied to every block (ZVC as in cDMA; BPC = DBX on
+ * every block; the best single encoding) -- PZ_CAND_ZVC, PZ_CAND_DBX, ...
+ * reproduce those columns on the same data. Arguments, buffers, capacity and
+ * errors as pz_compress; a mask with bits outside PZ_CAND_ALL gives
+ * PZ_ERR_ARG. */
+pz_status pz_compress_candidates(const void *d_in, size_t nbytes, int elem_width,
+                                 unsigned int candidates, void *d_out,
+                                 size_t out_capacity,
+                                 unsigned long long *d_total_bytes,
+                                 pz_stream_t stream);
+
+/* Compressed sizes only: no stream is written and no scratch is used.
+ * Visits chunks 0, s, 2s, ... (s = chunk_stride >= 1) and reports
+ *   d_sizes[k]  (device, u16, ceil(C/s) entries; may be NULL): the size L of
+ *               chunk k*s, exactly the header pz_compress_candidates writes
+ *               for it with the same candidates;
+ *   *d_total    (device u64): the sum over the visited chunks of 2 + L, i.e.
+ *               the full stream length 2*C + sum(L) when s = 1 (the total
+ *               pz_compress reports), or UINT64_MAX if a device-side wait
+ *               timed out.
+ * With s > 1 the ratio estimate is (raw bytes of the visited chunks) /
+ * *d_total; the host knows the former: s = 4 on tensors above 32 MB is the
+ * paper's sampling.
+ * Source: Section III-B "Compressibility Predictor" (the engine reports a
+ * tensor's compressed size as the sum of its chunk headers; tensors that are
+ * not swapped are measured in a profiling iteration that compresses into a
+ * scratch buffer and discards the output -- this computes the same sizes
+ * without the output) and Section IV "Methodology", "Tensor capture"
+ * (tensors above 32 MB are compressed on every fourth 4 KB chunk).
+ *   d_in, nbytes, elem_width, candidates: as pz_compress_candidates.
+ * Errors: PZ_ERR_ARG (null/misaligned d_in with nbytes > 0, null d_total,
+ * elem_width <= 0, chunk_stride == 0, bad mask), PZ_ERR_CUDA. */
+pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width,
+                             unsigned int candidates, unsigned int chunk_stride,
+                             unsigned short *d_sizes,
+                             unsigned long long *d_total, pz_stream_t stream);
+
 /* Largest input pz_compress_noalloc accepts: 256 MiB (65,536 chunks). */
 #define PZ_NOALLOC_MAX_BYTES ((size_t)256 << 20)
 

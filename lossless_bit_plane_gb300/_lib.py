@@ -1,7 +1,8 @@
 """ctypes binding of ``libplanezip.so`` — argument marshalling only.
 
 The functions mirror the C ABI in ``include/planezip.h`` one to one
-(``pz_max_compressed_bytes``, ``pz_compress``, ``pz_decompress``); every step
+(``pz_max_compressed_bytes``, ``pz_compress``, ``pz_decompress``,
+``pz_compress_candidates``, ``pz_compressed_size``, ``pz_compress_noalloc``); every step
 of the codec runs in the library's CUDA kernels. The ``*_tensor`` helpers
 below use PyTorch only to allocate device memory and to name the current
 stream. There is no fallback: if the library is missing or cannot be loaded,
@@ -17,7 +18,11 @@ LIB_PATH = Path(__file__).resolve().parent / "libplanezip.so"
 PZ_OK, PZ_ERR_ARG, PZ_ERR_CAPACITY, PZ_ERR_CORRUPT, PZ_ERR_CUDA, PZ_ERR_TIMEOUT = range(6)
 STATUS_NAMES = {0: "PZ_OK", 1: "PZ_ERR_ARG", 2: "PZ_ERR_CAPACITY", 3: "PZ_ERR_CORRUPT",
                 4: "PZ_ERR_CUDA", 5: "PZ_ERR_TIMEOUT"}
-EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress", "pz_compress_noalloc")
+EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress", "pz_compress_candidates",
+           "pz_compressed_size", "pz_compress_noalloc")
+# candidate masks (bit t = tag t: ZVC 0, DBX 1, BX 2, ZBX 3, raw 4; raw is always allowed)
+PZ_CAND_ZVC, PZ_CAND_DBX, PZ_CAND_BX, PZ_CAND_ZBX, PZ_CAND_RAW = 0x01, 0x02, 0x04, 0x08, 0x10
+PZ_CAND_ALL = 0x1F
 NOALLOC_MAX_BYTES = 256 << 20  # PZ_NOALLOC_MAX_BYTES
 
 _lib = None
@@ -45,6 +50,10 @@ def load() -> ctypes.CDLL:
         L.pz_decompress.restype = ctypes.c_int
         L.pz_compress_noalloc.argtypes = [vp, sz, ctypes.c_int, vp, sz, vp, vp]
         L.pz_compress_noalloc.restype = ctypes.c_int
+        L.pz_compress_candidates.argtypes = [vp, sz, ctypes.c_int, ctypes.c_uint, vp, sz, vp, vp]
+        L.pz_compress_candidates.restype = ctypes.c_int
+        L.pz_compressed_size.argtypes = [vp, sz, ctypes.c_int, ctypes.c_uint, ctypes.c_uint, vp, vp, vp]
+        L.pz_compressed_size.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -74,6 +83,18 @@ def pz_compress_noalloc(d_in: int, nbytes: int, elem_width: int, d_out: int, out
                                           d_total_bytes or None, stream or None))
 
 
+def pz_compress_candidates(d_in: int, nbytes: int, elem_width: int, candidates: int, d_out: int,
+                           out_capacity: int, d_total_bytes: int, stream: int = 0) -> int:
+    return int(load().pz_compress_candidates(d_in or None, nbytes, elem_width, candidates, d_out or None,
+                                             out_capacity, d_total_bytes or None, stream or None))
+
+
+def pz_compressed_size(d_in: int, nbytes: int, elem_width: int, candidates: int, chunk_stride: int,
+                       d_sizes: int, d_total: int, stream: int = 0) -> int:
+    return int(load().pz_compressed_size(d_in or None, nbytes, elem_width, candidates, chunk_stride,
+                                         d_sizes or None, d_total or None, stream or None))
+
+
 # ---------------------------------------------------------------- torch glue
 
 def _current_stream_handle(device) -> int:
@@ -82,7 +103,7 @@ def _current_stream_handle(device) -> int:
     return int(torch.cuda.current_stream(device).cuda_stream)
 
 
-def compress_tensor(x, elem_width: int, out=None, total=None):
+def compress_tensor(x, elem_width: int, out=None, total=None, candidates: int = PZ_CAND_ALL):
     """Compress the bytes of a contiguous CUDA tensor.
 
     Returns ``(out, total)``: ``out`` is a uint8 CUDA tensor of
@@ -99,11 +120,36 @@ def compress_tensor(x, elem_width: int, out=None, total=None):
         out = torch.empty(max(cap, 16), dtype=torch.uint8, device=x.device)
     if total is None:
         total = torch.empty(1, dtype=torch.int64, device=x.device)
-    rc = pz_compress(x.data_ptr(), nbytes, elem_width, out.data_ptr(), out.numel(), total.data_ptr(),
-                     _current_stream_handle(x.device))
+    rc = pz_compress_candidates(x.data_ptr(), nbytes, elem_width, candidates, out.data_ptr(), out.numel(),
+                                total.data_ptr(), _current_stream_handle(x.device))
     if rc != PZ_OK:
-        raise PlaneZipError("pz_compress", rc)
+        raise PlaneZipError("pz_compress_candidates", rc)
     return out, total
+
+
+def compressed_size_tensor(x, elem_width: int, chunk_stride: int = 1, candidates: int = PZ_CAND_ALL,
+                           with_sizes: bool = True):
+    """Sizes only (no stream): returns ``(sizes, total)``. ``sizes`` is a
+    uint16-valued int32 CUDA tensor of ceil(C / chunk_stride) entries (None
+    when ``with_sizes`` is false); ``total`` is a 1-element int64 CUDA tensor
+    with the sum of 2 + L over the visited chunks. Asynchronous."""
+    import torch
+
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("compressed_size_tensor needs a contiguous CUDA tensor")
+    nbytes = x.numel() * x.element_size()
+    C = (nbytes + 4095) // 4096
+    n = (C + chunk_stride - 1) // chunk_stride
+    sizes = torch.zeros(max(n, 1), dtype=torch.int16, device=x.device) if with_sizes else None
+    total = torch.empty(1, dtype=torch.int64, device=x.device)
+    rc = pz_compressed_size(x.data_ptr(), nbytes, elem_width, candidates, chunk_stride,
+                            sizes.data_ptr() if sizes is not None else 0, total.data_ptr(),
+                            _current_stream_handle(x.device))
+    if rc != PZ_OK:
+        raise PlaneZipError("pz_compressed_size", rc)
+    if sizes is not None:
+        sizes = sizes[:n].to(torch.int32) & 0xFFFF
+    return sizes, total
 
 
 def decompress_tensor(stream_buf, comp_bytes: int, elem_width: int, nbytes: int, out=None, status=None):

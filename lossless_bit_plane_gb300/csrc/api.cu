@@ -28,7 +28,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  int enc_ctas_per_sm[2] = {0, 0};
+  int enc_ctas_per_sm[4] = {0, 0, 0, 0};  // [2 * size_only + w16]
 };
 
 std::mutex g_mu;
@@ -47,13 +47,16 @@ cudaError_t device_info(DeviceInfo &out) {
     if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     for (int w = 0; w < 2; ++w) {
       const size_t smem = pz::encode_smem_bytes(w == 1);
-      const void *k = pz::encode_kernel_ptr(w == 1);
-      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-        return e;
-      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.enc_ctas_per_sm[w], k, pz::encode_threads(),
-                                                             smem)) != cudaSuccess)
-        return e;
-      if (d.enc_ctas_per_sm[w] < 1) return cudaErrorInvalidConfiguration;
+      for (int so = 0; so < 2; ++so) {
+        const void *k = pz::encode_kernel_ptr(w == 1, so == 1);
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+          return e;
+        int n = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, pz::encode_threads(), smem)) != cudaSuccess)
+          return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        d.enc_ctas_per_sm[2 * so + w] = n;
+      }
     }
     for (int w = 0; w < 2; ++w)
       if ((e = cudaFuncSetAttribute(pz::walk_kernel_ptr(w == 1), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -72,6 +75,36 @@ cudaError_t device_info(DeviceInfo &out) {
   return cudaSuccess;
 }
 
+// The 2D tensor map over the input (rows of 128 bytes; 32 x u32 each) and
+// the encoder launch. `units` is the number of chunks the launch visits
+// (every chunk, or every stride-th for sizes only); a.in, a.nbytes and
+// a.num_chunks are set by the caller.
+pz_status launch_encoder(pz::EncodeArgs &a, bool w16, bool size_only, size_t units, const DeviceInfo &info,
+                         cudaStream_t s) {
+  a.tma_rows = a.nbytes / 128;
+  alignas(64) CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  if (a.tma_rows > 0) {
+    cuuint64_t dims[2] = {32, (cuuint64_t)a.tma_rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t *>(a.in), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return PZ_ERR_CUDA;
+  }
+  const int warps = pz::encode_warps();
+  size_t grid = (size_t)info.enc_ctas_per_sm[2 * (size_only ? 1 : 0) + (w16 ? 1 : 0)] * info.sms;
+  const size_t need = (units + warps - 1) / warps;
+  if (grid > need) grid = need;
+  void *args[2] = {&tmap, &a};
+  if (cudaLaunchKernel(pz::encode_kernel_ptr(w16, size_only), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
+                       pz::encode_smem_bytes(w16), s) != cudaSuccess)
+    return PZ_ERR_CUDA;
+  return PZ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -83,7 +116,13 @@ size_t pz_max_compressed_bytes(size_t nbytes) {
 
 pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width, void *d_out, size_t out_capacity,
                       unsigned long long *d_total_bytes, pz_stream_t stream) {
-  if (elem_width <= 0 || !d_total_bytes) return PZ_ERR_ARG;
+  return pz_compress_candidates(d_in, nbytes, elem_width, PZ_CAND_ALL, d_out, out_capacity, d_total_bytes, stream);
+}
+
+pz_status pz_compress_candidates(const void *d_in, size_t nbytes, int elem_width, unsigned int candidates,
+                                 void *d_out, size_t out_capacity, unsigned long long *d_total_bytes,
+                                 pz_stream_t stream) {
+  if (elem_width <= 0 || !d_total_bytes || (candidates & ~PZ_CAND_ALL)) return PZ_ERR_ARG;
   const size_t C = num_chunks(nbytes);
   if (nbytes && (!d_in || !d_out)) return PZ_ERR_ARG;
   if (nbytes && (!aligned16(d_in) || !aligned16(d_out))) return PZ_ERR_ARG;
@@ -100,7 +139,7 @@ pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width, void *d_o
   uint8_t *scratch = out + align16(2 * C + nbytes);
   if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
 
-  pz::EncodeArgs a;
+  pz::EncodeArgs a{};
   a.in = static_cast<const uint8_t *>(d_in);
   a.out = out;
   a.status = reinterpret_cast<unsigned long long *>(scratch);
@@ -108,31 +147,33 @@ pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width, void *d_o
   a.total = d_total_bytes;
   a.nbytes = nbytes;
   a.num_chunks = (uint32_t)C;
-  a.tma_rows = nbytes / 128;
+  a.candidates = candidates | PZ_CAND_RAW;
+  a.stride = 1;
+  return launch_encoder(a, elem_width == 2, false, C, info, s);
+}
 
-  alignas(64) CUtensorMap tmap;
-  std::memset(&tmap, 0, sizeof(tmap));
-  if (a.tma_rows > 0) {
-    cuuint64_t dims[2] = {32, (cuuint64_t)a.tma_rows};  // 32 x u32 per 128-byte row
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {32, 32};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(d_in), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return PZ_ERR_CUDA;
-  }
-
-  const bool w16 = (elem_width == 2);
-  const int warps = pz::encode_warps();
-  size_t grid = (size_t)info.enc_ctas_per_sm[w16 ? 1 : 0] * info.sms;
-  const size_t need = (C + warps - 1) / warps;
-  if (grid > need) grid = need;
-  void *args[2] = {&tmap, &a};
-  if (cudaLaunchKernel(pz::encode_kernel_ptr(w16), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
-                       pz::encode_smem_bytes(w16), s) != cudaSuccess)
-    return PZ_ERR_CUDA;
-  return PZ_OK;
+pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width, unsigned int candidates,
+                             unsigned int chunk_stride, unsigned short *d_sizes, unsigned long long *d_total,
+                             pz_stream_t stream) {
+  if (elem_width <= 0 || !d_total || chunk_stride == 0 || (candidates & ~PZ_CAND_ALL)) return PZ_ERR_ARG;
+  const size_t C = num_chunks(nbytes);
+  if (nbytes && !d_in) return PZ_ERR_ARG;
+  if (nbytes && !aligned16(d_in)) return PZ_ERR_ARG;
+  if (C > 0x7FFFFFFFu || nbytes / 128 > 0xFFFFFFFFull) return PZ_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_total, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
+  if (nbytes == 0) return PZ_OK;
+  DeviceInfo info;
+  if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
+  pz::EncodeArgs a{};
+  a.in = static_cast<const uint8_t *>(d_in);
+  a.total = d_total;
+  a.nbytes = nbytes;
+  a.num_chunks = (uint32_t)C;
+  a.candidates = candidates | PZ_CAND_RAW;
+  a.stride = chunk_stride;
+  a.sizes = d_sizes;
+  return launch_encoder(a, elem_width == 2, true, (C + chunk_stride - 1) / chunk_stride, info, s);
 }
 
 pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, void *d_out, size_t nbytes,
@@ -232,7 +273,7 @@ extern "C" pz_status pz_compress_noalloc(const void *d_in, size_t nbytes, int el
   // the previous call's look-back words and ticket must not leak into this one
   if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
 
-  pz::EncodeArgs a;
+  pz::EncodeArgs a{};
   a.in = static_cast<const uint8_t *>(d_in);
   a.out = static_cast<uint8_t *>(d_out);
   a.status = static_cast<unsigned long long *>(scratch);
@@ -240,28 +281,7 @@ extern "C" pz_status pz_compress_noalloc(const void *d_in, size_t nbytes, int el
   a.total = d_total_bytes;
   a.nbytes = nbytes;
   a.num_chunks = (uint32_t)C;
-  a.tma_rows = nbytes / 128;
-
-  alignas(64) CUtensorMap tmap;
-  std::memset(&tmap, 0, sizeof(tmap));
-  if (a.tma_rows > 0) {
-    cuuint64_t dims[2] = {32, (cuuint64_t)a.tma_rows};
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {32, 32};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(d_in), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return PZ_ERR_CUDA;
-  }
-  const bool w16 = (elem_width == 2);
-  const int warps = pz::encode_warps();
-  size_t grid = (size_t)info.enc_ctas_per_sm[w16 ? 1 : 0] * info.sms;
-  const size_t need = (C + warps - 1) / warps;
-  if (grid > need) grid = need;
-  void *args[2] = {&tmap, &a};
-  if (cudaLaunchKernel(pz::encode_kernel_ptr(w16), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
-                       pz::encode_smem_bytes(w16), s) != cudaSuccess)
-    return PZ_ERR_CUDA;
-  return PZ_OK;
+  a.candidates = PZ_CAND_ALL;
+  a.stride = 1;
+  return launch_encoder(a, elem_width == 2, false, C, info, s);
 }

@@ -127,24 +127,21 @@ struct Sizes {
   Plan win;            // its plan (plane candidates only)
 };
 
-__device__ __forceinline__ void select_min(const Sizes &z, uint32_t &tag, uint32_t &bits);
-
-// Pick the smallest candidate (ties to the lowest tag) and keep its plan.
-__device__ __forceinline__ void keep_smallest(Sizes &z, const Plan &bx, const Plan &zbx, const Plan &dbx) {
-  select_min(z, z.tag, z.bits);
-  z.win = (z.tag == kTagZBX) ? zbx : (z.tag == kTagDBX) ? dbx : bx;
-}
-
-__device__ __forceinline__ void select_min(const Sizes &z, uint32_t &tag, uint32_t &bits) {
-  tag = 0;
-  int best = z.s[0];
+// Pick the smallest allowed candidate (bit t of cand = tag t; the raw block
+// is always allowed), ties to the lowest tag, and keep its plan.
+__device__ __forceinline__ void keep_smallest(Sizes &z, const Plan &bx, const Plan &zbx, const Plan &dbx,
+                                              uint32_t cand) {
+  uint32_t tag = kTagRAW;
+  int best = z.s[kTagRAW];
 #pragma unroll
-  for (int t = 1; t < 5; ++t)
-    if (z.s[t] < best) {
+  for (int t = 3; t >= 0; --t)
+    if (((cand >> t) & 1u) && z.s[t] <= best) {
       best = z.s[t];
-      tag = t;
+      tag = (uint32_t)t;
     }
-  bits = (uint32_t)best;
+  z.tag = tag;
+  z.bits = (uint32_t)best;
+  z.win = (tag == kTagZBX) ? zbx : (tag == kTagDBX) ? dbx : bx;
 }
 
 // The lane's block in its 128-byte row of the stage, as the TMA left it
@@ -181,7 +178,7 @@ __device__ __forceinline__ void load_block(uint32_t rowbase, uint32_t lane, uint
 // s: the block's 32 symbols. Returns the five candidate sizes (tag excluded).
 // The words are streamed from the stage row four at a time, so that only the
 // accumulators stay in registers.
-__device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
+__device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uint32_t cand) {
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0;  // BX
   uint32_t nz = 0, zn = 0, adjz = 0, last = 0;                            // ZBX / ZVC
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Bw = 0, gdprev = 0;  // DBX
@@ -261,7 +258,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
     const uint64_t Z = (uint64_t)(uint32_t)~ad | ((uint64_t)(Bw == 0) << 32);
     z.s[kTagDBX] = 32 + run_cost(Z, 5) + plan_cost(dbx, 31, 5) + plan_cost(tp, 31, 5);
   }
-  keep_smallest(z, bx, zbx, dbx);
+  keep_smallest(z, bx, zbx, dbx, cand);
   return z;
 }
 
@@ -269,7 +266,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane) {
 // sp: split-packed block (word j = symbol j | symbol j+32 << 16).
 // Split-packed words (word j = symbol j | symbol j+32 << 16) are built while
 // streaming the stage row: word j needs raw words j/2 and 16 + j/2.
-__device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane) {
+__device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uint32_t cand) {
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0, g0 = 0;
   uint32_t mlo = 0, mhi = 0, zn = 0, adjz = 0, last = 0, fst = 0, seen = 0;
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Blo = 0, Bhi = 0, gdprev = 0,
@@ -403,7 +400,7 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane) {
     const uint32_t Z = ~dbx.nz & 0x1FFFFu;
     z.s[kTagDBX] = 16 + run_cost(Z, 4) + plan_cost(dbx, 63, 6);
   }
-  keep_smallest(z, bx, zbx, dbx);
+  keep_smallest(z, bx, zbx, dbx, cand);
   return z;
 }
 
@@ -756,7 +753,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t u) {
   return r * 128u + ((u ^ (r & 7u)) << 4);
 }
 
-template <bool W16>
+// kSizeOnly: the sizes-only launch (no stream). It classifies chunks 0,
+// stride, 2*stride, ... (warps take them in a fixed round-robin, no ticket),
+// and reports each L and the sum of 2 + L, without emitting, locating or
+// writing any payload.
+template <bool W16, bool kSizeOnly>
 __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     encode_kernel(const __grid_constant__ CUtensorMap tmap, EncodeArgs p) {
   using Cfg = EncCfg<W16>;
@@ -808,17 +809,26 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     __syncwarp();
   };
 
-  uint32_t t = 0;
-  if (lane == 0) t = atomicAdd(p.ticket, 1u);
-  t = __shfl_sync(0xFFFFFFFFu, t, 0);
-  int cur = 0;
-  if (t < C) issue(t, cur);
+  // work units: chunk t itself, or (sizes only) chunk t * stride
+  const uint32_t U = kSizeOnly ? (C + p.stride - 1) / p.stride : C;
+  const uint32_t warp_id = blockIdx.x * kEncWarps + warp, nwarps = gridDim.x * kEncWarps;
+  auto next_unit = [&](uint32_t u) -> uint32_t {
+    if (kSizeOnly) return u + nwarps;
+    uint32_t v = 0;
+    if (lane == 0) v = atomicAdd(p.ticket, 1u);
+    return __shfl_sync(0xFFFFFFFFu, v, 0);
+  };
+  auto chunk_of = [&](uint32_t u) -> uint32_t { return kSizeOnly ? u * p.stride : u; };
+  unsigned long long size_sum = 0;  // sizes only: this warp's sum of 2 + L
 
-  while (t < C) {
-    uint32_t nt = 0;
-    if (lane == 0) nt = atomicAdd(p.ticket, 1u);
-    nt = __shfl_sync(0xFFFFFFFFu, nt, 0);
-    if (Cfg::kStages == 2 && nt < C) issue(nt, cur ^ 1);  // prefetch the next chunk
+  uint32_t u = kSizeOnly ? warp_id : next_unit(0);
+  int cur = 0;
+  if (u < U) issue(chunk_of(u), cur);
+
+  while (u < U) {
+    const uint32_t t = chunk_of(u);
+    const uint32_t nu = next_unit(u);
+    if (Cfg::kStages == 2 && nu < U) issue(chunk_of(nu), cur ^ 1);  // prefetch the next chunk
 
     uint8_t *st = stage0 + cur * 4096;
     if (uses_tma(t)) {
@@ -833,7 +843,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     const bool active = lane < nblk;
 
     const uint32_t rowbase = smem_u32(st) + lane * 128u;
-    Sizes z = W16 ? classify16(rowbase, lane) : classify32(rowbase, lane);
+    Sizes z = W16 ? classify16(rowbase, lane, p.candidates) : classify32(rowbase, lane, p.candidates);
     const uint32_t tag = z.tag;
     uint32_t bits = z.bits;
     bits = active ? bits + 3 : 0;
@@ -850,6 +860,17 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     uint32_t L = (total_bits + 7) >> 3;
     const bool raw_chunk = L >= raw_len;
     if (raw_chunk) L = raw_len;
+    if (kSizeOnly) {
+      if (lane == 0) {
+        if (p.sizes) p.sizes[u] = (uint16_t)L;
+        size_sum += 2u + L;
+      }
+      __syncwarp();
+      fence_proxy_async_smem();  // generic-proxy use of the stage before the next TMA write
+      u = nu;
+      if (u < U) issue(chunk_of(u), cur);
+      continue;
+    }
     if (lane == 0) st_relaxed_u64(p.status + t, (t == 0 ? kFlagInc : kFlagAgg) | L);
 
     if (!raw_chunk) {
@@ -886,25 +907,31 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
 
     __syncwarp();
     fence_proxy_async_smem();  // generic-proxy use of the stage before the next TMA write
-    t = nt;
+    u = nu;
     if (Cfg::kStages == 2)
       cur ^= 1;
-    else if (t < C)
-      issue(t, cur);  // one stage: load the next chunk now that this one is done
+    else if (u < U)
+      issue(chunk_of(u), cur);  // one stage: load the next chunk now that this one is done
   }
+  if (kSizeOnly && lane == 0 && size_sum) atomicAdd(p.total, size_sum);
   if (failed && lane == 0) atomicMax(p.total, ~0ull);
 }
 
-template __global__ void encode_kernel<false>(const __grid_constant__ CUtensorMap, EncodeArgs);
-template __global__ void encode_kernel<true>(const __grid_constant__ CUtensorMap, EncodeArgs);
+template __global__ void encode_kernel<false, false>(const __grid_constant__ CUtensorMap, EncodeArgs);
+template __global__ void encode_kernel<true, false>(const __grid_constant__ CUtensorMap, EncodeArgs);
+template __global__ void encode_kernel<false, true>(const __grid_constant__ CUtensorMap, EncodeArgs);
+template __global__ void encode_kernel<true, true>(const __grid_constant__ CUtensorMap, EncodeArgs);
 
 size_t encode_smem_bytes(bool w16) { return w16 ? EncCfg<true>::kBytes : EncCfg<false>::kBytes; }
 int encode_threads() { return kEncWarps * 32; }
 int encode_warps() { return kEncWarps; }
 
-const void *encode_kernel_ptr(bool w16) {
-  return w16 ? reinterpret_cast<const void *>(&encode_kernel<true>)
-             : reinterpret_cast<const void *>(&encode_kernel<false>);
+const void *encode_kernel_ptr(bool w16, bool size_only) {
+  if (size_only)
+    return w16 ? reinterpret_cast<const void *>(&encode_kernel<true, true>)
+               : reinterpret_cast<const void *>(&encode_kernel<false, true>);
+  return w16 ? reinterpret_cast<const void *>(&encode_kernel<true, false>)
+             : reinterpret_cast<const void *>(&encode_kernel<false, false>);
 }
 
 }  // namespace pz

@@ -17,6 +17,11 @@ struct EncodeArgs {
   uint64_t nbytes;
   uint64_t tma_rows;             // 128-byte rows covered by the tensor map (0: none)
   uint32_t num_chunks;
+  uint32_t candidates;           // allowed block candidates (bit t = tag t; raw always)
+  // size-only launches: chunks 0, stride, 2*stride, ... ; sizes[k] = L of
+  // chunk k*stride (when not null); *total += sum of 2 + L
+  uint32_t stride;
+  uint16_t *sizes;
 };
 
 struct DecodeArgs {
@@ -31,7 +36,7 @@ struct DecodeArgs {
 size_t encode_smem_bytes(bool w16);
 int encode_threads();
 int encode_warps();
-const void *encode_kernel_ptr(bool w16);
+const void *encode_kernel_ptr(bool w16, bool size_only);
 
 int walk_threads();
 size_t walk_smem_bytes();

@@ -61,7 +61,7 @@ int pzo_compress(const uint8_t *in, size_t nbytes, int elem_width,
  * in `candidates` (bit t = tag t; raw is always allowed): the smallest
  * allowed candidate is kept, ties to the lowest tag. PZO_CAND_ALL gives
  * pzo_compress. This reproduces the paper's single-encoding comparisons
- * (Section IV-B, Fig. 3: ZVC only, BPC = DBX on every block, ...). */
+ * (Section V-A "Compression Ratio", Fig. 3: ZVC only, BPC = DBX on every block, ...). */
 int pzo_compress_candidates(const uint8_t *in, size_t nbytes, int elem_width, unsigned candidates,
                             uint8_t *out, size_t cap, size_t *total);
 

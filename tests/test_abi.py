@@ -22,7 +22,7 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(pz_\w+)\s*\(", text)))
 
 
-def test_header_declares_the_three_entry_points():
+def test_header_declares_every_entry_point():
     assert declared_functions() == sorted(_lib.EXPORTS)
 
 
@@ -51,6 +51,23 @@ def test_compress_argument_errors_are_host_side(lib):
     assert _lib.pz_compress(FAKE_IN + 4, n, 4, FAKE_OUT, cap, FAKE_WORD) == _lib.PZ_ERR_ARG
     assert _lib.pz_compress(FAKE_IN, n, 4, FAKE_OUT + 8, cap, FAKE_WORD) == _lib.PZ_ERR_ARG
     assert _lib.pz_compress(FAKE_IN, n, 4, FAKE_OUT, cap - 1, FAKE_WORD) == _lib.PZ_ERR_CAPACITY
+
+
+def test_candidates_and_size_argument_errors_are_host_side(lib):
+    n = 8192
+    cap = _lib.pz_max_compressed_bytes(n)
+    # mask bits outside PZ_CAND_ALL
+    assert _lib.pz_compress_candidates(FAKE_IN, n, 4, 0x20, FAKE_OUT, cap, FAKE_WORD) == _lib.PZ_ERR_ARG
+    assert _lib.pz_compress_candidates(FAKE_IN, n, 0, _lib.PZ_CAND_ZVC, FAKE_OUT, cap, FAKE_WORD) == _lib.PZ_ERR_ARG
+    assert _lib.pz_compress_candidates(FAKE_IN, n, 4, _lib.PZ_CAND_DBX, FAKE_OUT, cap - 1,
+                                       FAKE_WORD) == _lib.PZ_ERR_CAPACITY
+    size = _lib.pz_compressed_size
+    assert size(FAKE_IN, n, 4, _lib.PZ_CAND_ALL, 0, 0, FAKE_WORD) == _lib.PZ_ERR_ARG      # stride 0
+    assert size(FAKE_IN, n, 4, _lib.PZ_CAND_ALL, 1, 0, 0) == _lib.PZ_ERR_ARG              # no total
+    assert size(FAKE_IN, n, 0, _lib.PZ_CAND_ALL, 1, 0, FAKE_WORD) == _lib.PZ_ERR_ARG      # width
+    assert size(FAKE_IN, n, 4, 0x40, 1, 0, FAKE_WORD) == _lib.PZ_ERR_ARG                  # mask
+    assert size(0, n, 4, _lib.PZ_CAND_ALL, 1, 0, FAKE_WORD) == _lib.PZ_ERR_ARG            # no input
+    assert size(FAKE_IN + 4, n, 4, _lib.PZ_CAND_ALL, 1, 0, FAKE_WORD) == _lib.PZ_ERR_ARG  # misaligned
 
 
 def test_decompress_argument_errors_are_host_side(lib):

@@ -1,7 +1,7 @@
 """Pins of the oracle's restricted block selection (candidate masks).
 
 The paper compares PlaneZip with single encodings applied to every block
-(Section IV-B, Fig. 3: ZVC, BPC = DBX on every block, the best single
+(Section V-A, Fig. 3: ZVC, BPC = DBX on every block, the best single
 encoding). A candidate mask (bit t = tag t) restricts the per-block choice;
 the raw block always stays allowed, and a chunk that would grow is still
 stored raw (Section III-A "Stream format"). What pins it, independently of
