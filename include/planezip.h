@@ -158,6 +158,56 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width,
                              unsigned short *d_sizes,
                              unsigned long long *d_total, pz_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * The compressed swap path. A tensor is swapped out to host memory as
+ * PlaneZip streams and swapped back in from them; the codec and the host
+ * link work at the same time (Section III-A: the engine compresses
+ * device-to-host swaps and decompresses host-to-device ones; Section III-C,
+ * Equation 2: a transfer is limited by the link or by the engine, whichever
+ * is slower). The tensor is cut into pieces of piece_bytes (a multiple of
+ * 4096); piece k+1 is coded on `stream` while piece k is on the link (an
+ * internal copy stream of the call). Host memory should be pinned for the
+ * copies to overlap (pageable memory works, serialised). These calls block
+ * the host (the sizes of the pieces are needed on the host) and cannot be
+ * captured in a CUDA graph.
+ *
+ * Container written by pz_swap_out (little-endian): a 32-byte head (u32
+ * "PZSW", u32 pieces, u64 nbytes, u64 piece_bytes, u32 elem_width, u32 0),
+ * one u64 stream length per piece, then each piece's pz_compress stream,
+ * each starting at a 16-byte boundary.
+ * ---------------------------------------------------------------------- */
+
+/* Device staging bytes both calls need for piece_bytes (0 if piece_bytes is
+ * not a positive multiple of 4096): two pieces' largest streams plus the
+ * encoder's scratch. Host-only, pure. */
+size_t pz_swap_work_bytes(size_t piece_bytes);
+
+/* Host bytes pz_swap_out may write for nbytes in pieces of piece_bytes
+ * (0 for an invalid piece size). Host-only, pure. */
+size_t pz_swap_capacity(size_t nbytes, size_t piece_bytes);
+
+/* Swap out nbytes at d_in (device, 16-byte aligned) into the container at
+ * h_out (host, h_capacity >= pz_swap_capacity). d_work: device, 16-byte
+ * aligned, work_bytes >= pz_swap_work_bytes(piece_bytes). Returns when the
+ * container is complete; *h_total (host) = its length.
+ * Errors: PZ_ERR_ARG (bad pointer, width, piece size), PZ_ERR_CAPACITY,
+ * PZ_ERR_TIMEOUT (a device-side wait of the encoder timed out), PZ_ERR_CUDA. */
+pz_status pz_swap_out(const void *d_in, size_t nbytes, int elem_width,
+                      size_t piece_bytes, void *d_work, size_t work_bytes,
+                      void *h_out, size_t h_capacity, size_t *h_total,
+                      pz_stream_t stream);
+
+/* Swap in: decode the container of h_bytes at h_in (host) back into nbytes
+ * at d_out (device, 16-byte aligned). The container's head must match
+ * nbytes and its piece lengths must lie inside h_bytes (else PZ_ERR_ARG,
+ * nothing enqueued). d_work as for pz_swap_out with the container's piece
+ * size. Returns once the copies are done and the decodes are enqueued on
+ * `stream`; *d_status (device int) becomes PZ_OK or PZ_ERR_CORRUPT when
+ * the stream completes. */
+pz_status pz_swap_in(const void *h_in, size_t h_bytes, void *d_work,
+                     size_t work_bytes, void *d_out, size_t nbytes,
+                     int *d_status, pz_stream_t stream);
+
 /* Largest input pz_compress_noalloc accepts: 256 MiB (65,536 chunks). */
 #define PZ_NOALLOC_MAX_BYTES ((size_t)256 << 20)
 

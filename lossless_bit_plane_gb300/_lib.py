@@ -2,7 +2,8 @@
 
 The functions mirror the C ABI in ``include/planezip.h`` one to one
 (``pz_max_compressed_bytes``, ``pz_compress``, ``pz_decompress``,
-``pz_compress_candidates``, ``pz_compressed_size``, ``pz_compress_noalloc``); every step
+``pz_compress_candidates``, ``pz_compressed_size``, the swap path ``pz_swap_*`` and
+``pz_compress_noalloc``); every step
 of the codec runs in the library's CUDA kernels. The ``*_tensor`` helpers
 below use PyTorch only to allocate device memory and to name the current
 stream. There is no fallback: if the library is missing or cannot be loaded,
@@ -19,7 +20,8 @@ PZ_OK, PZ_ERR_ARG, PZ_ERR_CAPACITY, PZ_ERR_CORRUPT, PZ_ERR_CUDA, PZ_ERR_TIMEOUT 
 STATUS_NAMES = {0: "PZ_OK", 1: "PZ_ERR_ARG", 2: "PZ_ERR_CAPACITY", 3: "PZ_ERR_CORRUPT",
                 4: "PZ_ERR_CUDA", 5: "PZ_ERR_TIMEOUT"}
 EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress", "pz_compress_candidates",
-           "pz_compressed_size", "pz_compress_noalloc")
+           "pz_compressed_size", "pz_swap_work_bytes", "pz_swap_capacity", "pz_swap_out", "pz_swap_in",
+           "pz_compress_noalloc")
 # candidate masks (bit t = tag t: ZVC 0, DBX 1, BX 2, ZBX 3, raw 4; raw is always allowed)
 PZ_CAND_ZVC, PZ_CAND_DBX, PZ_CAND_BX, PZ_CAND_ZBX, PZ_CAND_RAW = 0x01, 0x02, 0x04, 0x08, 0x10
 PZ_CAND_ALL = 0x1F
@@ -54,6 +56,14 @@ def load() -> ctypes.CDLL:
         L.pz_compress_candidates.restype = ctypes.c_int
         L.pz_compressed_size.argtypes = [vp, sz, ctypes.c_int, ctypes.c_uint, ctypes.c_uint, vp, vp, vp]
         L.pz_compressed_size.restype = ctypes.c_int
+        L.pz_swap_work_bytes.argtypes = [sz]
+        L.pz_swap_work_bytes.restype = sz
+        L.pz_swap_capacity.argtypes = [sz, sz]
+        L.pz_swap_capacity.restype = sz
+        L.pz_swap_out.argtypes = [vp, sz, ctypes.c_int, sz, vp, sz, vp, sz, ctypes.POINTER(sz), vp]
+        L.pz_swap_out.restype = ctypes.c_int
+        L.pz_swap_in.argtypes = [vp, sz, vp, sz, vp, sz, vp, vp]
+        L.pz_swap_in.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -93,6 +103,29 @@ def pz_compressed_size(d_in: int, nbytes: int, elem_width: int, candidates: int,
                        d_sizes: int, d_total: int, stream: int = 0) -> int:
     return int(load().pz_compressed_size(d_in or None, nbytes, elem_width, candidates, chunk_stride,
                                          d_sizes or None, d_total or None, stream or None))
+
+
+def pz_swap_work_bytes(piece_bytes: int) -> int:
+    return int(load().pz_swap_work_bytes(piece_bytes))
+
+
+def pz_swap_capacity(nbytes: int, piece_bytes: int) -> int:
+    return int(load().pz_swap_capacity(nbytes, piece_bytes))
+
+
+def pz_swap_out(d_in: int, nbytes: int, elem_width: int, piece_bytes: int, d_work: int, work_bytes: int,
+                h_out: int, h_capacity: int, stream: int = 0) -> tuple[int, int]:
+    """Returns (status, container length written at h_out)."""
+    total = ctypes.c_size_t(0)
+    rc = load().pz_swap_out(d_in or None, nbytes, elem_width, piece_bytes, d_work or None, work_bytes,
+                            h_out or None, h_capacity, ctypes.byref(total), stream or None)
+    return int(rc), int(total.value)
+
+
+def pz_swap_in(h_in: int, h_bytes: int, d_work: int, work_bytes: int, d_out: int, nbytes: int, d_status: int,
+               stream: int = 0) -> int:
+    return int(load().pz_swap_in(h_in or None, h_bytes, d_work or None, work_bytes, d_out or None, nbytes,
+                                 d_status or None, stream or None))
 
 
 # ---------------------------------------------------------------- torch glue
@@ -168,3 +201,40 @@ def decompress_tensor(stream_buf, comp_bytes: int, elem_width: int, nbytes: int,
     if rc != PZ_OK:
         raise PlaneZipError("pz_decompress", rc)
     return out, status
+
+
+class SwapBuffers:
+    """Device staging and a pinned host container for swapping tensors of up
+    to ``max_bytes`` bytes in pieces of ``piece_bytes`` (torch allocations;
+    the swap itself runs in the library)."""
+
+    def __init__(self, max_bytes: int, piece_bytes: int = 16 << 20, device="cuda"):
+        import torch
+
+        self.piece_bytes = piece_bytes
+        self.work_bytes = pz_swap_work_bytes(piece_bytes)
+        if self.work_bytes == 0:
+            raise ValueError("piece_bytes must be a positive multiple of 4096")
+        self.work = torch.empty(self.work_bytes, dtype=torch.uint8, device=device)
+        self.host = torch.empty(pz_swap_capacity(max_bytes, piece_bytes), dtype=torch.uint8).pin_memory()
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def swap_out(self, x, elem_width: int) -> int:
+        """Container length; the container is in ``self.host[:length]``."""
+        nbytes = x.numel() * x.element_size()
+        rc, total = pz_swap_out(x.data_ptr(), nbytes, elem_width, self.piece_bytes, self.work.data_ptr(),
+                                self.work_bytes, self.host.data_ptr(), self.host.numel(),
+                                _current_stream_handle(x.device))
+        if rc != PZ_OK:
+            raise PlaneZipError("pz_swap_out", rc)
+        return total
+
+    def swap_in(self, length: int, out):
+        """Decode the container back into ``out`` (asynchronous); returns the
+        device status tensor."""
+        nbytes = out.numel() * out.element_size()
+        rc = pz_swap_in(self.host.data_ptr(), length, self.work.data_ptr(), self.work_bytes, out.data_ptr(), nbytes,
+                        self.status.data_ptr(), _current_stream_handle(out.device))
+        if rc != PZ_OK:
+            raise PlaneZipError("pz_swap_in", rc)
+        return self.status

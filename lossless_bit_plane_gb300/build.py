@@ -17,7 +17,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = ROOT / "_build"
 LIB = PKG / "libplanezip.so"
-SOURCES = ("api.cu", "encode.cu", "decode.cu")
+SOURCES = ("api.cu", "encode.cu", "decode.cu", "swap.cu")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -178,6 +178,16 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width, un
 
 pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, void *d_out, size_t nbytes,
                         int *d_status, pz_stream_t stream) {
+  return pz::decompress_launch(d_in, comp_bytes, elem_width, d_out, nbytes, d_status, stream, true);
+}
+
+}  // extern "C"
+
+// pz_decompress's checks and launches; with reset_status false the device
+// status word is not cleared first, so that several streams (the pieces of
+// a swapped tensor) accumulate their errors into one word.
+pz_status pz::decompress_launch(const void *d_in, size_t comp_bytes, int elem_width, void *d_out, size_t nbytes,
+                                int *d_status, pz_stream_t stream, bool reset_status) {
   if (elem_width <= 0 || !d_status) return PZ_ERR_ARG;
   const size_t C = num_chunks(nbytes);
   if (nbytes && (!d_in || !d_out)) return PZ_ERR_ARG;
@@ -185,7 +195,7 @@ pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, voi
   if (C > 0x7FFFFFFFu) return PZ_ERR_ARG;
   if (comp_bytes < 2 * C) return PZ_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d_status, 0, sizeof(int), s) != cudaSuccess) return PZ_ERR_CUDA;
+  if (reset_status && cudaMemsetAsync(d_status, 0, sizeof(int), s) != cudaSuccess) return PZ_ERR_CUDA;
   if (C == 0) return PZ_OK;
 
   pz::DecodeArgs a;
@@ -215,7 +225,6 @@ pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, voi
   return PZ_OK;
 }
 
-}  // extern "C"
 
 // ---------------------------------------------------------------------------
 // Allocation-free compress: the same encoder launch as pz_compress, with the

@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "planezip.h"
+
 namespace pz {
 
 struct EncodeArgs {
@@ -46,5 +48,10 @@ const void *size_sum_kernel_ptr();    // 256 threads, one block per group but th
 int decode_threads();
 int decode_chunks_per_cta();
 const void *decode_kernel_ptr(bool w16);
+
+// pz_decompress's body; reset_status false leaves *d_status as it is, so
+// that several calls accumulate their errors (atomicMax) in one word.
+pz_status decompress_launch(const void *d_in, size_t comp_bytes, int elem_width, void *d_out, size_t nbytes,
+                            int *d_status, pz_stream_t stream, bool reset_status);
 
 }  // namespace pz

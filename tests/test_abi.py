@@ -70,6 +70,58 @@ def test_candidates_and_size_argument_errors_are_host_side(lib):
     assert size(FAKE_IN + 4, n, 4, _lib.PZ_CAND_ALL, 1, 0, FAKE_WORD) == _lib.PZ_ERR_ARG  # misaligned
 
 
+def test_swap_sizes_closed_forms(lib):
+    assert _lib.pz_swap_work_bytes(0) == 0 and _lib.pz_swap_work_bytes(4097) == 0
+    for piece in (4096, 1 << 20, 16 << 20):
+        stage = (_lib.pz_max_compressed_bytes(piece) + 15) // 16 * 16
+        assert _lib.pz_swap_work_bytes(piece) == 2 * stage + 32
+    for n, piece in ((0, 4096), (1, 4096), (4096, 4096), (4097, 4096), (10 << 20, 1 << 20), (3 << 20, 2 << 20)):
+        k = (n + piece - 1) // piece
+        cap = (32 + 8 * k + 15) // 16 * 16
+        for i in range(k):
+            raw = min(piece, n - i * piece)
+            cap += (2 * ((raw + 4095) // 4096) + raw + 15) // 16 * 16
+        assert _lib.pz_swap_capacity(n, piece) == cap
+
+
+def test_swap_argument_and_container_errors_are_host_side(lib):
+    import ctypes
+    import struct
+
+    piece, n = 1 << 20, 3 << 20
+    work = _lib.pz_swap_work_bytes(piece)
+    host = ctypes.create_string_buffer(_lib.pz_swap_capacity(n, piece))
+    h = ctypes.addressof(host)
+    cap = len(host)
+    assert _lib.pz_swap_out(FAKE_IN, n, 4, 4095, FAKE_OUT, work, h, cap)[0] == _lib.PZ_ERR_ARG
+    assert _lib.pz_swap_out(FAKE_IN, n, 0, piece, FAKE_OUT, work, h, cap)[0] == _lib.PZ_ERR_ARG
+    assert _lib.pz_swap_out(FAKE_IN + 4, n, 4, piece, FAKE_OUT, work, h, cap)[0] == _lib.PZ_ERR_ARG
+    assert _lib.pz_swap_out(FAKE_IN, n, 4, piece, FAKE_OUT, work - 1, h, cap)[0] == _lib.PZ_ERR_CAPACITY
+    assert _lib.pz_swap_out(FAKE_IN, n, 4, piece, FAKE_OUT, work, h, cap - 1)[0] == _lib.PZ_ERR_CAPACITY
+    # an empty tensor needs no device at all: the container is its head
+    rc, total = _lib.pz_swap_out(0, 0, 4, piece, 0, 0, h, cap)
+    assert rc == _lib.PZ_OK and total == 32
+    assert struct.unpack_from("<IIQQII", host.raw, 0) == (0x57535A50, 0, 0, piece, 4, 0)
+    # swap-in rejects a container that does not match, before any device work
+    # a well-formed container of three 1 KB piece streams (>= 2 bytes per chunk of a 1 MiB piece)
+    head = struct.pack("<IIQQII", 0x57535A50, 3, n, piece, 4, 0) + struct.pack("<3Q", 1024, 1024, 1024)
+    ctypes.memmove(h, head, len(head))
+    ok_len = 64 + 3 * 1024
+    assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n + 1, FAKE_WORD) == _lib.PZ_ERR_ARG   # nbytes
+    assert _lib.pz_swap_in(h, 40, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG          # truncated
+    bad = struct.pack("<IIQQII", 0x57535A51, 3, n, piece, 4, 0)
+    ctypes.memmove(h, bad, len(bad))
+    assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG      # magic
+    ctypes.memmove(h, head, len(head))
+    ctypes.memmove(h + 32, struct.pack("<Q", 1 << 40), 8)                                            # length
+    assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG
+    ctypes.memmove(h + 32, struct.pack("<Q", 511), 8)                                                # < 2C
+    assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG
+    ctypes.memmove(h + 32, struct.pack("<Q", 1024), 8)
+    assert _lib.pz_swap_in(h, ok_len - 1, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG  # past the end
+    assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work - 1, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_CAPACITY
+
+
 def test_decompress_argument_errors_are_host_side(lib):
     n = 3 * 4096 + 5  # 4 chunks -> the stream has at least 8 bytes
     assert _lib.pz_decompress(FAKE_IN, 100, 0, FAKE_OUT, n, FAKE_WORD) == _lib.PZ_ERR_ARG
