@@ -331,6 +331,7 @@ def run_ours(args, rank: int, world: int, local: int):
     if not args.no_e2e:
         e2e = run_e2e(args, segs, d_out, d_back, d_tot, d_st, totals_host, dev, stream, world, dist)
     sizes = run_sizes(args, segs, d_in, totals_host, dev, stream)
+    swap = run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream)
 
     per_seg = []
     for i, t in enumerate(segs):
@@ -374,6 +375,7 @@ def run_ours(args, rank: int, world: int, local: int):
         "eq2": eq2(raw / comp, raw / (tc_ms * 1e-3) / 1e9),
         "size_only": sizes["size_only"],
         "ablation": sizes["ablation"],
+        "swap": swap,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -449,6 +451,57 @@ def run_sizes(args, segs, d_in, totals_host, dev, stream):
             row["planezip_with_32bit_symbols"] = round(graw / sum(tot[i] for i in idx), 4)
         ablation[g] = row
     return {"size_only": size_only, "ablation": ablation}
+
+
+def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=16 << 20):
+    """Outside the headline's timed region: the compressed swap path
+    (pz_swap_out / pz_swap_in, 16 MiB pieces, pinned host memory) on a few
+    segments, against the plain pinned copy of the same bytes over the host
+    link, with the paper's Equation 2 evaluated on the measured numbers:
+    x_t = min(m/g, max(m/(c g), m/B)) with g the plain copy's rate, c the
+    ratio and B the codec's rate on that segment (raw bytes / kernel time)."""
+    import torch
+
+    from lossless_bit_plane_gb300 import _lib
+
+    pick = []
+    for pref in ("relu_fp32", "attention_bf16", "random"):
+        pick += [i for i, t in enumerate(segs) if t.name.startswith(pref)][:1]
+    if not pick:
+        return None
+    nmax = max(segs[i].nbytes for i in pick)
+    h_raw = torch.empty(nmax, dtype=torch.uint8).pin_memory()
+    bufs = _lib.SwapBuffers(nmax, piece, dev)
+    back = torch.empty(nmax, dtype=torch.uint8, device=dev)
+
+    def wall(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    rows = []
+    for i in pick:
+        t, x = segs[i], d_in[i]
+        n = t.nbytes
+        g_out = n / wall(lambda: h_raw[:n].copy_(x, non_blocking=True)) / 1e9
+        g_in = n / wall(lambda: back[:n].copy_(h_raw[:n], non_blocking=True)) / 1e9
+        length = bufs.swap_out(x, t.elem_width)
+        s_out = n / wall(lambda: bufs.swap_out(x, t.elem_width)) / 1e9
+        s_in = n / wall(lambda: bufs.swap_in(length, back[:n])) / 1e9
+        ok = int(bufs.status.item()) == 0 and torch.equal(back[:n], x)
+        c = n / totals_host[i]
+        b_c, b_d = n / (t_c[i] * 1e-3) / 1e9, n / (t_d[i] * 1e-3) / 1e9
+        eq2 = lambda g, b: 1.0 / min(1.0 / g, max(1.0 / (c * g), 1.0 / b))  # noqa: E731  (GB/s of raw bytes)
+        rows.append({"segment": t.name, "ratio": round(c, 4), "container_bytes": length,
+                     "link_d2h_gbs": round(g_out, 1), "link_h2d_gbs": round(g_in, 1),
+                     "swap_out_gbs": round(s_out, 1), "swap_in_gbs": round(s_in, 1),
+                     "eq2_out_gbs": round(eq2(g_out, b_c), 1), "eq2_in_gbs": round(eq2(g_in, b_d), 1),
+                     "round_trip_exact": ok})
+    return {"piece_bytes": piece, "unit": "GB/s of raw bytes", "host_memory": "pinned", "segments": rows}
 
 
 def run_e2e(args, segs, d_out, d_back, d_tot, d_st, totals_host, dev, stream, world, dist):

@@ -214,10 +214,17 @@ pz_status pz::decompress_launch(const void *d_in, size_t comp_bytes, int elem_wi
   if (groups > 1 && cudaLaunchKernel(pz::size_sum_kernel_ptr(), dim3((unsigned)(groups - 1)), dim3(256), args, 0,
                                      s) != cudaSuccess)
     return PZ_ERR_CUDA;
-  const size_t wt = (size_t)pz::walk_threads();
-  if (cudaLaunchKernel(pz::walk_kernel_ptr(w16), dim3((unsigned)((C + wt - 1) / wt)), dim3((unsigned)wt), args,
-                       pz::walk_smem_bytes(), s) != cudaSuccess)
-    return PZ_ERR_CUDA;
+  if (C <= pz::coop_max_chunks()) {  // small input: a warp walks each chunk
+    const size_t cw = (size_t)pz::coop_warps();
+    if (cudaLaunchKernel(pz::walk_coop_kernel_ptr(w16), dim3((unsigned)((C + cw - 1) / cw)), dim3((unsigned)(32 * cw)),
+                         args, pz::coop_smem_bytes(), s) != cudaSuccess)
+      return PZ_ERR_CUDA;
+  } else {  // a thread walks each chunk
+    const size_t wt = (size_t)pz::walk_threads();
+    if (cudaLaunchKernel(pz::walk_kernel_ptr(w16), dim3((unsigned)((C + wt - 1) / wt)), dim3((unsigned)wt), args,
+                         pz::walk_smem_bytes(), s) != cudaSuccess)
+      return PZ_ERR_CUDA;
+  }
   const size_t per = (size_t)pz::decode_chunks_per_cta();
   if (cudaLaunchKernel(pz::decode_kernel_ptr(w16), dim3((unsigned)((C + per - 1) / per)),
                        dim3(pz::decode_threads()), args, 0, s) != cudaSuccess)

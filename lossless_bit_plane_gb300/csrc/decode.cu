@@ -632,6 +632,137 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
   }
 }
 
+// ------------------------------------------------ cooperative walk (small)
+//
+// For inputs of up to kCoopMaxChunks chunks the walk kernel above is bound
+// by one thread's chain through a whole chunk, whatever the input's size.
+// Here a warp walks one chunk instead: the chunk's payload is staged in
+// shared memory by one bulk copy, the warp steps through the blocks with
+// every value warp-uniform, and lane k tests the flag bit of the k-th code
+// ahead under the assumption that the codes are verbatim (1 + W bits each),
+// so one ballot skips up to 32 verbatim planes. It writes the same record
+// as the walk kernel (offset and block starts at the chunk's output region).
+
+constexpr uint32_t kCoopWarps = 8;
+constexpr uint32_t kCoopStageBytes = 4096 + 32;  // a payload from its 16-byte unit, plus slack
+constexpr uint32_t kCoopStageWords = kCoopStageBytes / 4;
+constexpr uint32_t kCoopSmem = kCoopWarps * kCoopStageBytes + kCoopWarps * 8;
+constexpr uint32_t kCoopMaxChunks = 8192;
+
+// Sum of the sizes of chunks [0, c) for any c, by a warp (group sums of
+// whole groups, then 16-byte units of headers, then the last few headers).
+__device__ __forceinline__ unsigned long long sizes_before_chunk(const DecodeArgs &p, uint32_t c, uint32_t lane) {
+  const uint32_t g0 = c / kGroupChunks;
+  unsigned long long part = 0;
+  for (uint32_t g = lane; g < g0; g += 32)
+    part += *reinterpret_cast<const unsigned long long *>(p.out + (uint64_t)g * kGroupChunks * 4096u + kGroupSumAt);
+  const uint4 *h4 = reinterpret_cast<const uint4 *>(p.in);
+  const uint32_t u1 = c / 8;
+  for (uint32_t i = g0 * (kGroupChunks / 8) + lane; i < u1; i += 32) part += sum8_sizes(__ldg(h4 + i));
+  if (lane < (c & 7u)) part += __ldg(reinterpret_cast<const uint16_t *>(p.in) + 8u * u1 + lane);
+  return warp_sum_u64(part);
+}
+
+template <bool W16>
+__global__ void __launch_bounds__(kCoopWarps * 32)
+    walk_coop_kernel(DecodeArgs p) {
+  constexpr uint32_t w = W16 ? 16u : 32u;   // bits per symbol = BX planes
+  constexpr uint32_t N = W16 ? 64u : 32u;   // symbols per block
+  constexpr uint32_t K = W16 ? 4u : 5u;     // run field
+  extern __shared__ __align__(128) uint8_t coop_smem[];
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t C = p.num_chunks;
+  const uint32_t c = blockIdx.x * kCoopWarps + warp;
+  if (c >= C) return;
+  const uint32_t *stage = reinterpret_cast<const uint32_t *>(coop_smem + warp * kCoopStageBytes);
+  const uint32_t mb = smem_u32(coop_smem + kCoopWarps * kCoopStageBytes) + warp * 8u;
+  const uint64_t off = 2ull * C + sizes_before_chunk(p, c, lane);
+  const uint32_t L = __ldg(reinterpret_cast<const uint16_t *>(p.in) + c);
+  const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
+  if (L == 0 || L > raw_len || off + L > p.comp_bytes) {
+    if (lane == 0) atomicMax(p.status, kErrCorrupt);
+    return;
+  }
+  if (raw_len < kRecordBytes) return;  // the decode warp handles it
+  uint8_t *rec = p.out + (uint64_t)c * 4096u;
+  if (lane == 0) *reinterpret_cast<unsigned long long *>(rec) = off;
+  if (L == raw_len) return;  // raw chunk: the offset is all the decoder needs
+
+  const uint64_t a0 = off & ~15ull;
+  const uint32_t bytes = (uint32_t)(((off + L + 15) & ~15ull) - a0);  // <= 4112
+  if (lane == 0) {
+    mbar_init(mb, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive_expect_tx(mb, bytes);
+    bulk_load(smem_u32(stage), p.in + a0, bytes, mb);
+  }
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait(mb, 0, kMbarPolls))) {
+    mbar_wait(mb, 0, kMbarPolls);  // leave no copy in flight
+    if (lane == 0) atomicMax(p.status, kErrTimeout);
+    return;
+  }
+  const uint32_t bit0 = (uint32_t)(off - a0) * 8u;
+  // word indices are clamped to the stage: a malformed stream cannot read
+  // outside it (valid streams never reach the clamp)
+  auto word = [&](uint32_t i) { return stage[min(i, kCoopStageWords - 1u)]; };
+  auto peek = [&](uint32_t pos) {
+    const uint32_t q = bit0 + pos, i = q >> 5;
+    return __funnelshift_r(word(i), word(i + 1), q & 31u);
+  };
+  const uint32_t cap = 8u * L;
+  const uint32_t nblk = (raw_len + 127u) >> 7;
+  uint16_t *rs = reinterpret_cast<uint16_t *>(rec + 8);  // start of block b at rs[b - 1]
+  uint32_t pos = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (uint32_t b = 0; b < nblk && ok; ++b) {
+    if (b && lane == 0) rs[b - 1] = (uint16_t)pos;
+    const uint32_t tag = peek(pos) & 7u;
+    if (tag > kTagRAW) {
+      ok = false;
+      break;
+    }
+    const uint32_t n = __popc(peek(pos + 3u)) + (W16 ? __popc(peek(pos + 35u)) : 0u);
+    const bool masked = (tag == kTagZVC) || (tag == kTagZBX);
+    pos += 3u + (masked ? (W16 ? 64u : 32u) : 0u) + ((tag == kTagZVC) ? n * w : 0u) + ((tag == kTagDBX) ? w : 0u) +
+           ((tag == kTagRAW) ? 1024u : 0u);
+    const bool planes = (tag == kTagBX) || (tag == kTagDBX) || (tag == kTagZBX && n != 0);
+    const int top = (tag == kTagDBX) ? (int)w : (int)w - 1;
+    const uint32_t W = (tag == kTagDBX) ? N - 1u : (tag == kTagZBX) ? n : N;
+    const uint32_t S = 1u + W, pf = ceil_log2_u32(W);
+    int i = planes ? top : -1;
+#pragma unroll 1
+    while (i >= 0) {
+      const uint32_t q = bit0 + pos + lane * S;
+      const uint32_t f = __ballot_sync(0xFFFFFFFFu, (word(q >> 5) >> (q & 31u)) & 1u);
+      int m = (f == 0xFFFFFFFFu) ? 32 : __ffs(~f) - 1;  // leading verbatim codes
+      m = min(m, i + 1);
+      if (m > 0) {
+        pos += (uint32_t)m * S;
+        i -= m;
+        continue;
+      }
+      const uint32_t v0 = peek(pos);
+      const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4: the code is not verbatim
+      const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
+      const int rl = (tz == 1u) ? 2 + (int)((v0 >> 2) & ((1u << K) - 1u)) : 1;
+      if (rl > i + 1 || (tz == 4u && (v0 & 16u) && i == top)) {
+        ok = false;
+        break;
+      }
+      pos += len;
+      i -= rl;
+    }
+    if (pos > cap) ok = false;
+  }
+  if (ok && cap - pos >= 8) ok = false;
+  if (ok && cap > pos && (peek(pos) & ((1u << (cap - pos)) - 1u))) ok = false;
+  if (!ok && lane == 0) atomicMax(p.status, kErrCorrupt);
+}
+
 // Byte offset of 16-byte unit u of row r in a 128-byte-swizzled 4 KB tile.
 __device__ __forceinline__ uint32_t tile_swz(uint32_t r, uint32_t u) { return r * 128u + ((u ^ (r & 7u)) << 4); }
 
@@ -754,11 +885,20 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
 }
 
 template __global__ void walk_kernel<false>(DecodeArgs);
+template __global__ void walk_coop_kernel<false>(DecodeArgs);
+template __global__ void walk_coop_kernel<true>(DecodeArgs);
 template __global__ void walk_kernel<true>(DecodeArgs);
 template __global__ void decode_kernel<false>(DecodeArgs);
 template __global__ void decode_kernel<true>(DecodeArgs);
 
 int walk_threads() { return kWalkWarps * 32; }
+uint32_t coop_max_chunks() { return kCoopMaxChunks; }
+int coop_warps() { return kCoopWarps; }
+size_t coop_smem_bytes() { return kCoopSmem; }
+const void *walk_coop_kernel_ptr(bool w16) {
+  return w16 ? reinterpret_cast<const void *>(&walk_coop_kernel<true>)
+             : reinterpret_cast<const void *>(&walk_coop_kernel<false>);
+}
 size_t walk_smem_bytes() { return kWalkSmem; }
 uint32_t group_chunks() { return kGroupChunks; }
 const void *size_sum_kernel_ptr() { return reinterpret_cast<const void *>(&size_sum_kernel); }

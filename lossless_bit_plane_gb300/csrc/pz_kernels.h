@@ -44,6 +44,10 @@ int walk_threads();
 size_t walk_smem_bytes();
 const void *walk_kernel_ptr(bool w16);
 uint32_t group_chunks();              // chunks per size-sum group
+uint32_t coop_max_chunks();           // inputs up to this many chunks use the cooperative walk
+int coop_warps();                     // chunks per cooperative-walk block (one warp each)
+size_t coop_smem_bytes();
+const void *walk_coop_kernel_ptr(bool w16);
 const void *size_sum_kernel_ptr();    // 256 threads, one block per group but the last
 int decode_threads();
 int decode_chunks_per_cta();

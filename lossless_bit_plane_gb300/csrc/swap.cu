@@ -22,6 +22,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "planezip.h"
 #include "pz_kernels.h"
@@ -40,28 +41,41 @@ bool piece_ok(size_t piece) { return piece >= 4096 && piece % 4096 == 0; }
 // encoder's scratch), then two stream-length words and one status word.
 size_t stage_bytes(size_t piece) { return align16(pz_max_compressed_bytes(piece)); }
 
-// Streams and events of one call, released on every exit path.
+// The copy stream and events of the swap calls, created once per device and
+// kept; a mutex per device serialises swap calls on that device (each call
+// blocks the host until its copies are done, so they would not overlap).
 struct Pipe {
   cudaStream_t copy = nullptr;
   cudaEvent_t coded[2] = {nullptr, nullptr};  // compute stream: piece coded (and its length copied)
   cudaEvent_t moved[2] = {nullptr, nullptr};  // copy stream: piece on the link done
   bool ok = false;
-  Pipe() {
-    ok = cudaStreamCreateWithFlags(&copy, cudaStreamNonBlocking) == cudaSuccess;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_pipe_mu[kMaxDevices];
+Pipe g_pipe[kMaxDevices];
+
+// The current device's pipe, with its mutex held by `lk`; null on failure.
+Pipe *device_pipe(std::unique_lock<std::mutex> &lk) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  lk = std::unique_lock<std::mutex>(g_pipe_mu[dev]);
+  Pipe &p = g_pipe[dev];
+  if (!p.ok) {
+    bool ok = cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking) == cudaSuccess;
     for (int i = 0; i < 2 && ok; ++i)
-      ok = cudaEventCreateWithFlags(&coded[i], cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&moved[i], cudaEventDisableTiming) == cudaSuccess;
+      ok = cudaEventCreateWithFlags(&p.coded[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p.moved[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return nullptr;
+    p.ok = true;
   }
-  ~Pipe() {
-    for (int i = 0; i < 2; ++i) {
-      if (coded[i]) cudaEventDestroy(coded[i]);
-      if (moved[i]) cudaEventDestroy(moved[i]);
-    }
-    if (copy) {
-      cudaStreamSynchronize(copy);
-      cudaStreamDestroy(copy);
-    }
-  }
+  return &p;
+}
+
+// Waits for the copy stream on every exit path of a call, so that no copy
+// of the call is still in flight when it returns.
+struct CopyDrain {
+  cudaStream_t s;
+  ~CopyDrain() { cudaStreamSynchronize(s); }
 };
 
 }  // namespace
@@ -104,8 +118,11 @@ pz_status pz_swap_out(const void *d_in, size_t nbytes, int elem_width, size_t pi
   if (n == 0) return PZ_OK;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  Pipe pp;
-  if (!pp.ok) return PZ_ERR_CUDA;
+  std::unique_lock<std::mutex> lk;
+  Pipe *pipe = device_pipe(lk);
+  if (!pipe) return PZ_ERR_CUDA;
+  Pipe &pp = *pipe;
+  CopyDrain drain{pp.copy};
   uint8_t *work = static_cast<uint8_t *>(d_work);
   const size_t sb = stage_bytes(piece_bytes);
   uint8_t *stage[2] = {work, work + sb};
@@ -177,8 +194,11 @@ pz_status pz_swap_in(const void *h_in, size_t h_bytes, void *d_work, size_t work
   if (cudaMemsetAsync(d_status, 0, sizeof(int), s) != cudaSuccess) return PZ_ERR_CUDA;
   if (n == 0) return PZ_OK;
 
-  Pipe pp;
-  if (!pp.ok) return PZ_ERR_CUDA;
+  std::unique_lock<std::mutex> lk;
+  Pipe *pipe = device_pipe(lk);
+  if (!pipe) return PZ_ERR_CUDA;
+  Pipe &pp = *pipe;
+  CopyDrain drain{pp.copy};
   uint8_t *work = static_cast<uint8_t *>(d_work);
   uint8_t *stage[2] = {work, work + sb};
   // the link may start as soon as the caller's earlier work is done

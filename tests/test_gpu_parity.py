@@ -186,6 +186,34 @@ def test_corrupt_streams_report_status():
             assert out == out_ref
 
 
+def test_corrupt_streams_report_status_above_the_cooperative_walk_size():
+    # 8,500 chunks: decompress walks chunks one thread each (inputs of up to
+    # 8,192 chunks take the cooperative warp walk, covered above). Bits are
+    # flipped in the payloads of the last chunks only; since chunks are
+    # independent, the oracle judges each flip on that chunk alone.
+    rng = np.random.default_rng(29)
+    data = W.relu_values(8500 * 1024 - 77, rng).view(np.uint8)
+    n = data.size
+    s = bytearray(oracle.compress(data, 4))
+    lens, offs = chunk_table(bytes(s), n)
+    C = lens.size
+    st, back = gpu_decompress(bytes(s), n, 4)
+    assert st == 0 and back == data.tobytes()
+    for _ in range(24):
+        c = int(rng.integers(C - 12, C))
+        L = int(lens[c])
+        bad = bytearray(s)
+        bit = int(rng.integers(0, 8 * L))
+        bad[offs[c] + bit // 8] ^= 1 << (bit % 8)
+        st, out = gpu_decompress(bytes(bad), n, 4)
+        piece = data[4096 * c: 4096 * c + 4096]
+        mini = int(L).to_bytes(2, "little") + bytes(bad[offs[c]: offs[c] + L])
+        rc_ref, out_ref = oracle.decompress_status(mini, piece.size, 4)
+        assert st == rc_ref, (c, bit)
+        if st == 0:
+            assert out[4096 * c: 4096 * c + piece.size] == out_ref
+
+
 def test_repeated_calls_and_streams_are_deterministic():
     t = W.relu_fp32_4mib()
     x = to_device(t.data)
