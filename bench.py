@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--cpu-sample-mib", type=float, default=4.0,
                     help="MiB per segment timed through the CPU oracle")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the sizes-only, ablation and swap sections (run after the timed region)")
     ap.add_argument("--workload", default="sweep",
                     help="'sweep' (the 1 GiB sweep, the headline) or one sweep segment as <kind>_<dtype>, "
                          "e.g. attention_fp32, conv_bf16, random_u32 (used for small profiling cases)")
@@ -330,8 +332,9 @@ def run_ours(args, rank: int, world: int, local: int):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, segs, d_out, d_back, d_tot, d_st, totals_host, dev, stream, world, dist)
-    sizes = run_sizes(args, segs, d_in, totals_host, dev, stream)
-    swap = run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream)
+    sizes = {"size_only": None, "ablation": None} if args.no_extras else run_sizes(args, segs, d_in, totals_host, dev,
+                                                                                      stream)
+    swap = None if args.no_extras else run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream)
 
     per_seg = []
     for i, t in enumerate(segs):

@@ -465,7 +465,11 @@ __device__ __forceinline__ uint32_t bit_insert(uint32_t f, uint32_t v, uint32_t 
 constexpr uint32_t kWalkWarps = 2;
 constexpr uint32_t kWinUnits = 48;
 constexpr uint32_t kWinWords = kWinUnits * 4;
-constexpr uint32_t kWalkSmem = kWalkWarps * 32 * kWinUnits * 16 + kWalkWarps * 8;
+// windows are laid out kWinStride words apart (4 words more than a window,
+// a 16-byte multiple for the bulk copies) so that lanes reading the same
+// window offset -- as they all do right after a refill -- hit different banks
+constexpr uint32_t kWinStride = kWinWords + 4;
+constexpr uint32_t kWalkSmem = kWalkWarps * 32 * kWinStride * 4 + kWalkWarps * 8;
 
 // The warp's walk: lane = chunk. It is one loop that every lane runs until
 // the last lane is done (lanes that are done, or have nothing to walk, idle
@@ -593,8 +597,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     walk_kernel(DecodeArgs p) {
   extern __shared__ __align__(128) uint8_t walk_smem[];
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  const uint32_t *win = reinterpret_cast<const uint32_t *>(walk_smem) + (warp * 32u + lane) * kWinWords;
-  const uint32_t mb = smem_u32(walk_smem + kWalkWarps * 32 * kWinUnits * 16) + warp * 8u;
+  const uint32_t *win = reinterpret_cast<const uint32_t *>(walk_smem) + (warp * 32u + lane) * kWinStride;
+  const uint32_t mb = smem_u32(walk_smem + kWalkWarps * 32 * kWinStride * 4) + warp * 8u;
   const uint32_t C = p.num_chunks;
   const uint32_t first = (blockIdx.x * kWalkWarps + warp) * 32u;
   if (first >= C) return;
