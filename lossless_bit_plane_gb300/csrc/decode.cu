@@ -453,12 +453,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(mbar) : "memory");
 }
-// f with bit k replaced by bit 0 of v
-__device__ __forceinline__ uint32_t bit_insert(uint32_t f, uint32_t v, uint32_t k) {
-  uint32_t r;
-  asm("bfi.b32 %0, %1, %2, %3, 1;" : "=r"(r) : "r"(v), "r"(f), "r"(k));
-  return r;
-}
 
 // Walk kernel shape: warps of 32 chunks (lane = chunk); each lane reads its
 // chunk through a window of kWinUnits 16-byte units in shared memory.
@@ -536,13 +530,15 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
     // bit in the window; the clamp only binds for lanes that are done (a
     // walking lane re-based its window above), and keeps every read inside
     const uint32_t ql = min(qa - wbase, kWinUnits * 128u - kAhead);
-    uint32_t f = 0;
+    // flag k: bit t_k of the window, rotated to position k (the rotations
+    // are independent, and an OR tree joins them)
+    uint32_t y[kSkip];
 #pragma unroll
     for (uint32_t k = 1; k < kSkip; ++k) {
       const uint32_t t = ql + k * S;
-      const uint32_t x = win[t >> 5];
-      f = bit_insert(f, __funnelshift_r(x, x, t), k);
+      y[k] = __funnelshift_r(win[t >> 5], win[t >> 5], t - k) & (1u << k);
     }
+    uint32_t f = ((y[1] | y[2]) | (y[3] | y[4])) | ((y[5] | y[6]) | y[7]);
     const uint32_t wi = ql >> 5, sh = ql & 31u;
     const uint32_t x0 = win[wi], x1 = win[wi + 1], x2 = win[wi + 2], x3 = win[wi + 3];
     const uint32_t v0 = __funnelshift_r(x0, x1, sh), v1 = __funnelshift_r(x1, x2, sh), v2 = __funnelshift_r(x2, x3, sh);
@@ -741,7 +737,9 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
 #pragma unroll 1
     while (i >= 0) {
       const uint32_t q = bit0 + pos + lane * S;
-      const uint32_t f = __ballot_sync(0xFFFFFFFFu, (word(q >> 5) >> (q & 31u)) & 1u);
+      const uint32_t fw = word(q >> 5);
+      const uint32_t v0 = peek(pos);  // loaded with the flags: one round of loads per step
+      const uint32_t f = __ballot_sync(0xFFFFFFFFu, (fw >> (q & 31u)) & 1u);
       int m = (f == 0xFFFFFFFFu) ? 32 : __ffs(~f) - 1;  // leading verbatim codes
       m = min(m, i + 1);
       if (m > 0) {
@@ -749,7 +747,6 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         i -= m;
         continue;
       }
-      const uint32_t v0 = peek(pos);
       const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4: the code is not verbatim
       const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
       const int rl = (tz == 1u) ? 2 + (int)((v0 >> 2) & ((1u << K) - 1u)) : 1;
