@@ -489,9 +489,9 @@ def run_sizes(args, segs, d_in, totals_host, dev, stream):
     return {"size_only": size_only, "ablation": ablation}
 
 
-def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=16 << 20):
+def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=64 << 20):
     """Outside the headline's timed region: the compressed swap path
-    (pz_swap_out / pz_swap_in, 16 MiB pieces, pinned host memory) on a few
+    (pz_swap_out / pz_swap_in, 64 MiB pieces, pinned host memory) on a few
     segments, against the plain pinned copy of the same bytes over the host
     link, with the paper's Equation 2 evaluated on the measured numbers:
     x_t = min(m/g, max(m/(c g), m/B)) with g the plain copy's rate, c the

@@ -208,7 +208,7 @@ class SwapBuffers:
     to ``max_bytes`` bytes in pieces of ``piece_bytes`` (torch allocations;
     the swap itself runs in the library)."""
 
-    def __init__(self, max_bytes: int, piece_bytes: int = 16 << 20, device="cuda"):
+    def __init__(self, max_bytes: int, piece_bytes: int = 64 << 20, device="cuda"):
         import torch
 
         self.piece_bytes = piece_bytes
