@@ -195,7 +195,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
     andx &= g;
     gprev = g;
     const uint32_t m = x ? 0xFFFFFFFFu : 0u;
-    nz |= m & (1u << k);
+    nz = __funnelshift_r(nz, m, 1);  // word k's flag enters at bit 31; after 32 words it sits at bit k
     zn |= ~g & m;  // some survivor has a 0 in the plane
     adjz |= last & g;
     last = x ? g : last;
@@ -204,7 +204,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
       const uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);  // hi: borrow mask
       const uint32_t gd = lo ^ __funnelshift_r(lo, hi, 1);
       ord |= lo;
-      Bw |= hi & (1u << (k - 1));
+      Bw = __funnelshift_r(Bw, hi, 1);  // borrow of delta k ends at bit k (bit 0 stays 0)
       cd |= bd & gd;
       bd |= ad & gd;
       ad |= gd;
@@ -229,6 +229,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
     step(q.z, 4 * u + 2);
     step(q.w, 4 * u + 3);
   }
+  Bw >>= 1;  // borrow of delta k at bit k-1
   Sizes z;
   z.m0 = nz;
   z.m1 = 0;
@@ -270,7 +271,7 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0, g0 = 0;
   uint32_t mlo = 0, mhi = 0, zn = 0, adjz = 0, last = 0, fst = 0, seen = 0;
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Blo = 0, Bhi = 0, gdprev = 0,
-           gd0 = 0;
+           gd0 = 0, d32b = 0;
   const uint32_t s31lo = stage_unit(rowbase, lane, 3).w & 0xFFFF0000u;  // symbol 31 in the high half
   uint32_t xprev = 0;
   // split-packed word j >= 1 (symbols j and j+32); the loop below runs over
@@ -285,8 +286,8 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     andx &= g;
     gprev = g;
     const uint32_t m = halfmask_nonzero(x);
-    mlo |= (m & 1u) << j;
-    mhi |= (m >> 31) << j;
+    mlo = __funnelshift_r(mlo, m, 1);  // symbol j's flag enters at bit 31, ends at bit j
+    mhi = __funnelshift_l(m, mhi, 1);  // symbol j+32's flag enters at bit 0 (reversed below)
     zn |= ~g & m;
     adjz |= last & g;
     last = (g & m) | (last & ~m);
@@ -303,8 +304,8 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     andd &= gd;
     adjd |= gdprev & gd;
     gdprev = gd;
-    Blo |= ((bo >> 15) & 1u) << (j - 1);  // d_j -> position j-1
-    Bhi |= (bo >> 31) << (j - 1);         // d_{j+32} -> position j+31
+    Blo = __funnelshift_r(Blo, bo >> 15, 1);  // d_j's borrow ends at bit j (shifted to j-1 below)
+    Bhi = __funnelshift_l(bo, Bhi, 1);        // d_{j+32}'s borrow enters at bit 0 (reversed below)
     xprev = x;
   };
   {
@@ -318,7 +319,7 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     andx = g;
     gprev = g;
     const uint32_t m = halfmask_nonzero(x);
-    mlo = m & 1u;
+    mlo = m << 31;
     mhi = m >> 31;
     zn = ~g & m;
     last = g & m;
@@ -334,7 +335,8 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     andd = gd | 0x0000FFFFu;
     gd0 = gd;
     gdprev = gd;
-    Blo = bo;  // d_32's borrow -> plane position 31
+    Blo = 0;  // d_32's borrow (bo bit 31) goes to plane position 31 after the loop
+    d32b = bo;
     xprev = x;
     step(prmt(qa.x, qb.x, 0x7632u), 1);
     step(prmt(qa.y, qb.y, 0x5410u), 2);
@@ -350,6 +352,11 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     step(prmt(a1, b1, 0x5410u), 4u * h + 2u);
     step(prmt(a1, b1, 0x7632u), 4u * h + 3u);
   }
+  // the accumulations above left word j's bits at j (low halves) or 31 - j
+  // (high halves); bring them to the plane positions the masks use
+  mhi = __brev(mhi);
+  Blo = (Blo >> 1) | d32b;
+  Bhi = __brev(Bhi) >> 1;
   // combine the two halves (symbols 0..31 and 32..63) into 16-plane masks
   auto lo = [](uint32_t v) { return v & 0xFFFFu; };
   auto hi = [](uint32_t v) { return v >> 16; };
