@@ -39,10 +39,12 @@ WORKLOAD = ("1 GiB throughput sweep: {ReLU, smooth conv, causal attention} x {FP
             "at 128 MiB each + 256 MiB uniform u32; one compress call per segment, then all "
             "segments decompressed, back to back on one stream")
 
-# DRAM bytes per launch of the dominant kernel from one ncu capture
-# (profiles/ summary named for the kernel and workload). None until a capture
-# of the current kernel exists.
-NCU_TRAFFIC_BYTES_PER_LAUNCH = None
+# DRAM bytes (read + write) per encoder launch on the 1 GiB sweep: the mean
+# over its seven segments of dram__bytes_read.sum + dram__bytes_write.sum, one
+# ncu capture per segment workload (profiles/dram_bytes_per_kernel_sweep_segments.md).
+# It describes the current encode kernel only; it is reported when the sweep's
+# dominant call is the encoder and null otherwise.
+NCU_TRAFFIC_BYTES_PER_LAUNCH = 208.27e6
 
 
 def parse():
@@ -399,7 +401,8 @@ def run_ours(args, rank: int, world: int, local: int):
         "ratio": raw / comp,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_kind": peak_kind,
-                     "traffic": NCU_TRAFFIC_BYTES_PER_LAUNCH,
+                     "traffic": (NCU_TRAFFIC_BYTES_PER_LAUNCH if dominant == "pz_encode" and args.workload == "sweep"
+                                 else None),
                      "encode_frac": comp_ach / peak, "decode_frac": dec_ach / peak},
         "cpu_baseline": cpu,
         "e2e": e2e,
