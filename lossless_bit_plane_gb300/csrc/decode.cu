@@ -822,21 +822,56 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
   __syncwarp();  // every lane has read the record before any output is written
 
   if (L == raw_len) {  // raw chunk: the warp copies it (source at any byte offset)
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(p.in);
-    const uint64_t nw = (p.comp_bytes + 3) / 4;
-    const uint32_t sh = (uint32_t)(off & 3) * 8;
-    for (uint32_t v = lane; v * 16 < raw_len; v += 32) {
-      const uint64_t wi = (off + 16ull * v) >> 2;
-      uint32_t w5[5];
+    // output unit v comes from aligned source units v and v+1 (16-byte
+    // loads), realigned by the chunk's byte offset within a unit, which is
+    // the same for the whole warp
+    const uint64_t a0 = off & ~15ull;
+    const uint32_t s = (uint32_t)(off - a0);
+    const uint32_t nunits = (uint32_t)((((off + raw_len + 15) & ~15ull) - a0) >> 4);
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.in + a0);
+    const uint32_t ws = s >> 2, bs = (s & 3u) * 8u;
+    // a lane's loads are issued four units at a time (eight 16-byte loads in
+    // flight), so that enough bytes are in flight to cover the memory latency
+    constexpr int kR = 4;
+#pragma unroll 1
+    for (uint32_t v0 = lane; v0 * 16 < raw_len; v0 += 32u * kR) {
+      uint4 As[kR], Bs[kR];
 #pragma unroll
-      for (int k = 0; k < 5; ++k) w5[k] = (wi + k < nw) ? __ldg(w + wi + k) : 0u;
-      uint32_t o[4];
+      for (int i = 0; i < kR; ++i) {
+        const uint32_t v = v0 + 32u * i;
+        As[i] = (v < nunits) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        Bs[i] = (v + 1 < nunits) ? __ldg(src + v + 1) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(w5[k], w5[k + 1], sh);
-      if (v * 16 + 16 <= raw_len) {
-        *reinterpret_cast<uint4 *>(dst + 16ull * v) = make_uint4(o[0], o[1], o[2], o[3]);
-      } else {
-        for (uint32_t b = 0; v * 16 + b < raw_len; ++b) dst[16ull * v + b] = (uint8_t)(o[b >> 2] >> ((b & 3) * 8));
+      for (int i = 0; i < kR; ++i) {
+        const uint32_t v = v0 + 32u * i;
+        if (v * 16 >= raw_len) break;
+        const uint4 A = As[i], B = Bs[i];
+        const uint32_t a[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+        uint32_t o[4];
+        switch (ws) {  // the same for every lane
+          case 0:
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k], a[k + 1], bs);
+            break;
+          case 1:
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 1], a[k + 2], bs);
+            break;
+          case 2:
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 2], a[k + 3], bs);
+            break;
+          default:
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 3], a[k + 4], bs);
+            break;
+        }
+        if (v * 16 + 16 <= raw_len) {
+          *reinterpret_cast<uint4 *>(dst + 16ull * v) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          for (uint32_t b = 0; v * 16 + b < raw_len; ++b) dst[16ull * v + b] = (uint8_t)(o[b >> 2] >> ((b & 3) * 8));
+        }
       }
     }
     return;
