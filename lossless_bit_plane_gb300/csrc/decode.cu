@@ -881,9 +881,17 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
   const uint64_t a0 = off & ~15ull;
   const uint32_t nunits = (uint32_t)((off + L + 15 - a0) >> 4);
   const uint32_t sbase = smem_u32(stage[warp]);
-  for (uint32_t u = lane; u < nunits; u += 32) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.in + a0) + u);
-    *reinterpret_cast<uint4 *>(&stage[warp][4 * u]) = v;
+  {  // loads four units at a time before their stores (more bytes in flight)
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.in + a0);
+#pragma unroll 1
+    for (uint32_t u0 = lane; u0 < nunits; u0 += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = (u0 + 32u * i < nunits) ? __ldg(src + u0 + 32u * i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (u0 + 32u * i < nunits) *reinterpret_cast<uint4 *>(&stage[warp][4 * (u0 + 32u * i)]) = v[i];
+    }
   }
   __syncwarp();
   const StageBits sb{sbase};
