@@ -56,20 +56,4 @@ constexpr int kOk = 0;
 constexpr int kErrCorrupt = 3;
 constexpr int kErrTimeout = 5;
 
-// Per-width constants. W16: 16-bit symbols, 64 per block.
-template <bool W16>
-struct Geo {
-  static constexpr int w = W16 ? 16 : 32;   // symbol bits
-  static constexpr int N = W16 ? 64 : 32;   // symbols per block
-  static constexpr int K = W16 ? 4 : 5;     // run-length field bits (P = w or w+1 planes)
-  static constexpr int pN = W16 ? 6 : 5;    // position bits for W = N (BX)
-  static constexpr int pN1 = W16 ? 6 : 5;   // position bits for W = N-1 (DBX)
-};
-
-__host__ __device__ constexpr inline int ceil_log2_int(int v) {
-  int k = 0;
-  while ((1 << k) < v) ++k;
-  return k;
-}
-
 }  // namespace pz
