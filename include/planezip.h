@@ -208,6 +208,20 @@ pz_status pz_swap_in(const void *h_in, size_t h_bytes, void *d_work,
                      size_t work_bytes, void *d_out, size_t nbytes,
                      int *d_status, pz_stream_t stream);
 
+/* Test hook for the bounded waits (not part of the codec; the paper has no
+ * counterpart). Runs pz_compress's encoder on nbytes (2..4096 chunks) with
+ * chunk 0 never taken, so that the look-back of chunk 1 waits on a status
+ * word nothing publishes. That wait gives up after its iteration limit
+ * (about a second) and the launch ends with *d_total_bytes = UINT64_MAX, the
+ * encoder's timeout report; the GPU context stays usable. Arguments and
+ * errors as pz_compress (C outside 2..4096 gives PZ_ERR_ARG); the contents
+ * of d_out are unspecified afterwards. */
+pz_status pz_test_lookback_timeout(const void *d_in, size_t nbytes,
+                                   int elem_width, void *d_out,
+                                   size_t out_capacity,
+                                   unsigned long long *d_total_bytes,
+                                   pz_stream_t stream);
+
 /* Largest input pz_compress_noalloc accepts: 256 MiB (65,536 chunks). */
 #define PZ_NOALLOC_MAX_BYTES ((size_t)256 << 20)
 

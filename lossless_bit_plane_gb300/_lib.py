@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "PZ_OK", 1: "PZ_ERR_ARG", 2: "PZ_ERR_CAPACITY", 3: "PZ_ERR_CO
                 4: "PZ_ERR_CUDA", 5: "PZ_ERR_TIMEOUT"}
 EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress", "pz_compress_candidates",
            "pz_compressed_size", "pz_swap_work_bytes", "pz_swap_capacity", "pz_swap_out", "pz_swap_in",
-           "pz_compress_noalloc")
+           "pz_test_lookback_timeout", "pz_compress_noalloc")
 # candidate masks (bit t = tag t: ZVC 0, DBX 1, BX 2, ZBX 3, raw 4; raw is always allowed)
 PZ_CAND_ZVC, PZ_CAND_DBX, PZ_CAND_BX, PZ_CAND_ZBX, PZ_CAND_RAW = 0x01, 0x02, 0x04, 0x08, 0x10
 PZ_CAND_ALL = 0x1F
@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
         L.pz_compress_candidates.restype = ctypes.c_int
         L.pz_compressed_size.argtypes = [vp, sz, ctypes.c_int, ctypes.c_uint, ctypes.c_uint, vp, vp, vp]
         L.pz_compressed_size.restype = ctypes.c_int
+        L.pz_test_lookback_timeout.argtypes = [vp, sz, ctypes.c_int, vp, sz, vp, vp]
+        L.pz_test_lookback_timeout.restype = ctypes.c_int
         L.pz_swap_work_bytes.argtypes = [sz]
         L.pz_swap_work_bytes.restype = sz
         L.pz_swap_capacity.argtypes = [sz, sz]
@@ -103,6 +105,14 @@ def pz_compressed_size(d_in: int, nbytes: int, elem_width: int, candidates: int,
                        d_sizes: int, d_total: int, stream: int = 0) -> int:
     return int(load().pz_compressed_size(d_in or None, nbytes, elem_width, candidates, chunk_stride,
                                          d_sizes or None, d_total or None, stream or None))
+
+
+def pz_test_lookback_timeout(d_in: int, nbytes: int, elem_width: int, d_out: int, out_capacity: int,
+                             d_total_bytes: int, stream: int = 0) -> int:
+    """Test hook: the encoder with chunk 0 never taken (its look-back wait
+    runs out); *d_total_bytes ends as UINT64_MAX."""
+    return int(load().pz_test_lookback_timeout(d_in or None, nbytes, elem_width, d_out or None, out_capacity,
+                                               d_total_bytes or None, stream or None))
 
 
 def pz_swap_work_bytes(piece_bytes: int) -> int:

@@ -152,6 +152,38 @@ pz_status pz_compress_candidates(const void *d_in, size_t nbytes, int elem_width
   return launch_encoder(a, elem_width == 2, false, C, info, s);
 }
 
+pz_status pz_test_lookback_timeout(const void *d_in, size_t nbytes, int elem_width, void *d_out, size_t out_capacity,
+                                   unsigned long long *d_total_bytes, pz_stream_t stream) {
+  if (elem_width <= 0 || !d_total_bytes || !d_in || !d_out) return PZ_ERR_ARG;
+  const size_t C = num_chunks(nbytes);
+  if (C < 2 || C > 4096) return PZ_ERR_ARG;
+  if (!aligned16(d_in) || !aligned16(d_out)) return PZ_ERR_ARG;
+  if (out_capacity < pz_max_compressed_bytes(nbytes)) return PZ_ERR_CAPACITY;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
+  DeviceInfo info;
+  if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
+  uint8_t *out = static_cast<uint8_t *>(d_out);
+  uint8_t *scratch = out + align16(2 * C + nbytes);
+  if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
+  // the ticket starts at 1: chunk 0 is never taken, so its status word is
+  // never published
+  static const unsigned int kOne = 1;
+  if (cudaMemcpyAsync(scratch + 8 * C, &kOne, sizeof(kOne), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PZ_ERR_CUDA;
+  pz::EncodeArgs a{};
+  a.in = static_cast<const uint8_t *>(d_in);
+  a.out = out;
+  a.status = reinterpret_cast<unsigned long long *>(scratch);
+  a.ticket = reinterpret_cast<unsigned int *>(scratch + 8 * C);
+  a.total = d_total_bytes;
+  a.nbytes = nbytes;
+  a.num_chunks = (uint32_t)C;
+  a.candidates = PZ_CAND_ALL;
+  a.stride = 1;
+  return launch_encoder(a, elem_width == 2, false, C, info, s);
+}
+
 pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width, unsigned int candidates,
                              unsigned int chunk_stride, unsigned short *d_sizes, unsigned long long *d_total,
                              pz_stream_t stream) {

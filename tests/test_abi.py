@@ -122,6 +122,17 @@ def test_swap_argument_and_container_errors_are_host_side(lib):
     assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work - 1, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_CAPACITY
 
 
+def test_timeout_hook_argument_errors_are_host_side(lib):
+    cap = _lib.pz_max_compressed_bytes(4096)
+    assert _lib.pz_test_lookback_timeout(FAKE_IN, 4096, 4, FAKE_OUT, cap, FAKE_WORD) == _lib.PZ_ERR_ARG  # 1 chunk
+    n = 4097 * 4096
+    assert _lib.pz_test_lookback_timeout(FAKE_IN, n, 4, FAKE_OUT, _lib.pz_max_compressed_bytes(n),
+                                         FAKE_WORD) == _lib.PZ_ERR_ARG  # over 4096 chunks
+    n = 8192
+    assert _lib.pz_test_lookback_timeout(FAKE_IN, n, 4, FAKE_OUT, _lib.pz_max_compressed_bytes(n) - 1,
+                                         FAKE_WORD) == _lib.PZ_ERR_CAPACITY
+
+
 def test_decompress_argument_errors_are_host_side(lib):
     n = 3 * 4096 + 5  # 4 chunks -> the stream has at least 8 bytes
     assert _lib.pz_decompress(FAKE_IN, 100, 0, FAKE_OUT, n, FAKE_WORD) == _lib.PZ_ERR_ARG
