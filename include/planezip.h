@@ -95,10 +95,12 @@ pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width,
  *   nbytes      the original size.
  *   d_status    device int: set to PZ_OK, or PZ_ERR_CORRUPT if any field of
  *               the stream is malformed (bad size, tag, code, position,
- *               overrun, non-zero padding). The output is then unspecified
- *               but no byte outside [0, nbytes) is written, and reads stay
- *               inside the 16-byte-aligned granules that [0, comp_bytes)
- *               touches.
+ *               overrun, non-zero padding), or PZ_ERR_TIMEOUT if a
+ *               device-side wait for a copy into shared memory hit its
+ *               iteration limit (the larger code wins). The output is then
+ *               unspecified but no byte outside [0, nbytes) is written, and
+ *               reads stay inside the 16-byte-aligned granules that
+ *               [0, comp_bytes) touches.
  * Errors: PZ_ERR_ARG (null/misaligned pointer, elem_width <= 0,
  * comp_bytes < 2*C), PZ_ERR_CUDA. */
 pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width,

@@ -199,7 +199,7 @@ def decompress_tensor(stream_buf, comp_bytes: int, elem_width: int, nbytes: int,
     """Decompress ``comp_bytes`` of a uint8 CUDA tensor into ``nbytes``.
 
     Returns ``(out, status)``; ``status`` is a 1-element int32 CUDA tensor
-    holding PZ_OK or PZ_ERR_CORRUPT once the stream completes."""
+    holding PZ_OK, PZ_ERR_CORRUPT or PZ_ERR_TIMEOUT once the stream completes."""
     import torch
 
     if out is None:
