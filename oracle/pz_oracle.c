@@ -1,5 +1,6 @@
 /*
- * PlaneZip block codec: plain, single-threaded CPU oracle.
+ * PlaneZip block codec: plain, single-threaded CPU oracle. It keeps no state
+ * between calls, so separate threads may run it on separate buffers.
  *
  * TEST INFRASTRUCTURE ONLY (see pz_oracle.h). It is written for a reader to
  * check against the paper by eye: every plane is an explicit array of bits,
@@ -332,7 +333,7 @@ static void encode_zvc(bitwriter *w, const uint32_t *s, geometry g) {
 /* DBX: the base symbol (R4), then the w+1 bit-planes of the N-1 deltas
  * (R5), with adjacent planes XORed. */
 static void encode_dbx(bitwriter *w, const uint32_t *s, geometry g) {
-  static planes pl;
+  planes pl;
   uint64_t d[MAX_SYMBOLS];
   uint64_t mod_mask = (1ull << (g.w + 1)) - 1;
   put_field(w, s[0], g.w);
@@ -343,7 +344,7 @@ static void encode_dbx(bitwriter *w, const uint32_t *s, geometry g) {
 
 /* BX: the w bit-planes of the symbols themselves, adjacent planes XORed. */
 static void encode_bx(bitwriter *w, const uint32_t *s, geometry g) {
-  static planes pl;
+  planes pl;
   uint64_t v[MAX_SYMBOLS];
   for (int j = 0; j < g.N; j++) v[j] = s[j];
   make_planes(&pl, v, g.N, g.w);
@@ -353,7 +354,7 @@ static void encode_bx(bitwriter *w, const uint32_t *s, geometry g) {
 /* ZBX: the N-bit zero mask, then BX over the n non-zero symbols compacted
  * to the front, each plane n bits wide (R6 for n = 0). */
 static void encode_zbx(bitwriter *w, const uint32_t *s, geometry g) {
-  static planes pl;
+  planes pl;
   uint64_t t[MAX_SYMBOLS];
   int n = 0;
   for (int k = 0; k < g.N; k++) put_bit(w, s[k] != 0);
@@ -426,7 +427,7 @@ static int model_plane_codes(const planes *pl) {
 }
 
 static void candidate_bits_by_model(const uint8_t *block, geometry g, int out[5]) {
-  static planes pl;
+  planes pl;
   uint32_t s[MAX_SYMBOLS];
   uint64_t v[MAX_SYMBOLS] = {0};
   block_to_symbols(block, g, s);
@@ -468,7 +469,7 @@ static int select_tag(const int bits[5], unsigned allowed) {
 /* ------------------------------------------------------------------ */
 
 static int decode_block(bitreader *r, geometry g, uint8_t *block) {
-  static planes pl;
+  planes pl;
   uint32_t s[MAX_SYMBOLS];
   int tag = (int)get_field(r, 3);
   if (r->overrun) return PZO_ERR_CORRUPT;

@@ -65,9 +65,10 @@ def test_reference_arm_runs_on_rank_zero_only():
 def test_reference_arm_prints_one_json_line():
     env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
     out = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference", "--workload",
-                          "relu_fp32", "--steps", "1", "--warmup", "0", "--cpu-sample-mib", "0.25"],
+                          "relu_fp32", "--steps", "1", "--warmup", "0", "--cpu-parallel-mib", "0.25"],
                          env=env, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-2000:]
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["cores"] >= 1

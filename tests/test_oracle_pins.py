@@ -231,6 +231,28 @@ def test_round_trip_multi_chunk_tensors():
         assert oracle.decompress(s, len(data), ew) == data
 
 
+def test_chunk_aligned_split_concatenates():
+    # Section III-A "Stream format": every 4 KB chunk is coded on its own, so
+    # splitting the input at chunk boundaries and compressing each piece gives
+    # the pieces' size tables and payloads, which concatenate (all tables,
+    # then all payloads) into the whole input's stream.
+    rng = np.random.default_rng(11)
+    data = np.concatenate([
+        W.relu_values(4096 * 3, rng).view(np.uint8), rng.integers(0, 256, 4096 * 2, dtype=np.uint8),
+        np.zeros(4096 * 2, np.uint8), W.f32_to_bf16_rne(W.gelu_values(4096 * 2 + 777, rng)).view(np.uint8)]).tobytes()
+    n = len(data)
+    C = (n + 4095) // 4096
+    for ew in (4, 2):
+        whole = oracle.compress(data, ew)
+        for cuts in ([0, C], [0, 1, C], [0, 3, 5, 8, C], list(range(C + 1))):
+            heads, bodies = [], []
+            for a, b in zip(cuts[:-1], cuts[1:]):
+                s = oracle.compress(data[4096 * a: min(n, 4096 * b)], ew)
+                heads.append(s[:2 * (b - a)])
+                bodies.append(s[2 * (b - a):])
+            assert b"".join(heads) + b"".join(bodies) == whole, (ew, cuts)
+
+
 def test_ratio_accounting_includes_tags_headers_and_padding():
     rng = np.random.default_rng(12)
     data = W.relu_values(5 * 1024 + 77, rng).tobytes()
