@@ -86,8 +86,10 @@ struct StageBits {
 
 // Decode the block whose tag is at stage bit q into o[32] (the block's 32
 // words in memory order); q advances past the block. Plane codes are parsed
-// by a per-plane loop that is the same instruction stream for every lane
-// (the code class picks values by selects, not branches): each plane is
+// by a per-plane loop; a verbatim code takes a short branch of its own (the
+// low planes of activations are verbatim in nearly every block, so whole
+// warps skip the classification there), the other codes pick their values
+// by selects rather than branches: each plane is
 // X_i, rebuilt to the pre-XOR plane P_i = X_i ^ P_{i+1} and stored in the
 // lane's row (FP32 plane i < 32 in word i; BF16 plane i < 16 in words i and
 // 16+i; DBX rows pre-shifted so row bit j is delta j). One 32x32 bit
@@ -171,16 +173,20 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
         const uint32_t a = sb.addr(q), sh = q & 31u;
         const uint32_t w0 = lds32d(a), w1 = lds32d(a + 4), w2 = lds32d(a + 8);
         const uint32_t lo = __funnelshift_r(w0, w1, sh), hi = __funnelshift_r(w1, w2, sh);
-        const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;
-        const uint32_t qf = (lo >> 5) & pmask;
-        const bool hi4 = (lo & 16u) != 0;
-        const uint32_t xv = __funnelshift_r(lo, hi, 1) & full;
-        const uint32_t xp = (hi4 ? 1u : 3u) << qf;
-        const uint32_t x5 = hi4 ? Pup : full;
-        X = (tz == 0u) ? xv : (tz == 3u) ? xp : (tz == 4u) ? x5 : 0u;
-        q += (tz == 4u) ? 5u : ((lens >> (7u * tz)) & 127u);
-        if (tz == 1u) run = 1 + (int)((lo >> 2) & ((1u << K) - 1u));
-        bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
+        if (lo & 1u) {  // verbatim: 1 + the plane
+          X = __funnelshift_r(lo, hi, 1) & full;
+          q += 1u + (uint32_t)W;
+        } else {
+          const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // 1..4
+          const uint32_t qf = (lo >> 5) & pmask;
+          const bool hi4 = (lo & 16u) != 0;
+          const uint32_t xp = (hi4 ? 1u : 3u) << qf;
+          const uint32_t x5 = hi4 ? Pup : full;
+          X = (tz == 3u) ? xp : (tz == 4u) ? x5 : 0u;
+          q += (tz == 4u) ? 5u : ((lens >> (7u * tz)) & 127u);
+          if (tz == 1u) run = 1 + (int)((lo >> 2) & ((1u << K) - 1u));
+          bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
+        }
       }
       const uint32_t Pi = (i == top) ? X : (X ^ Pup);
       Pup = Pi;
@@ -198,16 +204,20 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
         uint32_t b64;
         const uint64_t win = sb.peek64(q, b64);
         const uint32_t lo = (uint32_t)win;
-        const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;
-        const uint32_t qf = (lo >> 5) & pmask;
-        const bool hi4 = (lo & 16u) != 0;
-        const uint64_t xv = (W >= 64) ? ((win >> 1) | ((uint64_t)b64 << 63)) : ((win >> 1) & full);
-        const uint64_t xp = (hi4 ? 1ull : 3ull) << qf;
-        const uint64_t x5 = hi4 ? Pup : full;
-        X = (tz == 0u) ? xv : (tz == 3u) ? xp : (tz == 4u) ? x5 : 0ull;
-        q += (tz == 4u) ? 5u : ((lens >> (7u * tz)) & 127u);
-        if (tz == 1u) run = 1 + (int)((lo >> 2) & ((1u << K) - 1u));
-        bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
+        if (lo & 1u) {  // verbatim: 1 + the plane
+          X = (W >= 64) ? ((win >> 1) | ((uint64_t)b64 << 63)) : ((win >> 1) & full);
+          q += 1u + (uint32_t)W;
+        } else {
+          const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // 1..4
+          const uint32_t qf = (lo >> 5) & pmask;
+          const bool hi4 = (lo & 16u) != 0;
+          const uint64_t xp = (hi4 ? 1ull : 3ull) << qf;
+          const uint64_t x5 = hi4 ? Pup : full;
+          X = (tz == 3u) ? xp : (tz == 4u) ? x5 : 0ull;
+          q += (tz == 4u) ? 5u : ((lens >> (7u * tz)) & 127u);
+          if (tz == 1u) run = 1 + (int)((lo >> 2) & ((1u << K) - 1u));
+          bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
+        }
       }
       const uint64_t Pi = (i == top) ? X : (X ^ Pup);
       Pup = Pi;
@@ -466,19 +476,22 @@ constexpr uint32_t kWinStride = kWinWords + 4;
 constexpr uint32_t kWalkSmem = kWalkWarps * 32 * kWinStride * 4 + kWalkWarps * 8;
 
 // The warp's walk: lane = chunk. It is one loop that every lane runs until
-// the last lane is done (lanes that are done, or have nothing to walk, idle
-// through the selects), so that the warp stays converged: an iteration
-// either reads a block header (tag; the mask of ZVC / ZBX; the base of DBX)
-// and skips what needs no parsing, or advances over plane codes: it tests
-// the flag bits of the next eight codes under the assumption that they are
-// verbatim (1 + W bits each) and skips the m leading verbatim ones, or, when
-// the first code is not verbatim, classifies it by its leading zero bits
-// (stream order, capped at 4): 01 run (2+K bits, 2+field planes), 001
-// single zero (3), 0001x position code (5+p), 0000x all-ones / pre-XOR-zero
-// (5). A lane's window holds the units from the one under its position on;
-// when any lane's next iteration could read past its window, every walking
-// lane re-bases its window at its position with one bulk copy, and the warp
-// waits once for all of them. Records: the start bit of block b >= 1 goes to
+// the last lane is done (lanes that are done, or have nothing to walk, sit
+// out both steps). An iteration takes up to two steps per lane:
+//  - a header step, when the lane stands at a block: the tag, the mask of
+//    ZVC / ZBX or the base of DBX; what needs no parsing (ZVC symbols, a
+//    raw block) is skipped, and a block with plane codes goes on to
+//  - a plane step in the same iteration: at most one code that is not
+//    verbatim, classified by its leading zero bits (stream order, capped at
+//    4): 01 run (2+K bits, 2+field planes), 001 single zero (3), 0001x
+//    position code (5+p), 0000x all-ones / pre-XOR-zero (5); then the flag
+//    bits of the next kSkip codes are tested under the assumption that they
+//    are verbatim (1 + W bits each) and the m leading verbatim ones are
+//    skipped.
+// A lane's window holds the units from the one under its position on; when
+// any lane's next iteration could read past its window, every walking lane
+// re-bases its window at its position with one bulk copy, and the warp waits
+// once for all of them. Records: the start bit of block b >= 1 goes to
 // rs[b - 1]. Returns false where the chunk is malformed.
 template <bool W16>
 __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64_t off, uint32_t L, uint32_t nblk,
@@ -486,8 +499,13 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
   constexpr uint32_t w = W16 ? 16u : 32u;   // bits per symbol = BX planes
   constexpr uint32_t N = W16 ? 64u : 32u;   // symbols per block
   constexpr uint32_t K = W16 ? 4u : 5u;     // run field
-  constexpr uint32_t kSkip = 8;
-  constexpr uint32_t kAhead = (kSkip - 1) * (N + 1) + 128;  // bits an iteration may read past its position
+  constexpr uint32_t kSkip = W16 ? 6u : 10u;  // BF16 blocks have at most 7 verbatim planes in a row
+  // bits an iteration may read past its position: four (FP32) or five
+  // (BF16) words at the position, or a plane block's header fields (tag and
+  // mask, or tag and base), one code of at most 11 bits and kSkip flags
+  // N + 1 apart
+  constexpr uint32_t kPlaneReach = 3u + N + 11u + (kSkip - 1u) * (N + 1u) + 64u;
+  constexpr uint32_t kAhead = (kPlaneReach > 160u ? kPlaneReach : 160u) + 32u;
   const uint32_t lane = lane_id();
   const uint64_t a0 = off & ~15ull;
   const uint8_t *g0 = p.in + a0;
@@ -503,9 +521,11 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
   bool ok = true;
   bool run = walk;
 #pragma unroll 1
-  while (__any_sync(0xFFFFFFFFu, run)) {
+  while (true) {
     const uint32_t qa = bit0 + min(pos, cap);
-    if (__any_sync(0xFFFFFFFFu, run && qa + kAhead >= lim)) {
+    const bool need = run && qa + kAhead >= lim;
+    if (!__any_sync(0xFFFFFFFFu, run)) break;
+    if (__any_sync(0xFFFFFFFFu, need)) {
       fence_proxy_async_smem();  // this lane's reads of its window before the bulk write
       if (run) {
         const uint32_t u = qa >> 7;  // <= nunits
@@ -530,53 +550,68 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
     // bit in the window; the clamp only binds for lanes that are done (a
     // walking lane re-based its window above), and keeps every read inside
     const uint32_t ql = min(qa - wbase, kWinUnits * 128u - kAhead);
-    // flag k: bit t_k of the window, rotated to position k (the rotations
-    // are independent, and an OR tree joins them)
-    uint32_t y[kSkip];
-#pragma unroll
-    for (uint32_t k = 1; k < kSkip; ++k) {
-      const uint32_t t = ql + k * S;
-      y[k] = __funnelshift_r(win[t >> 5], win[t >> 5], t - k) & (1u << k);
-    }
-    uint32_t f = ((y[1] | y[2]) | (y[3] | y[4])) | ((y[5] | y[6]) | y[7]);
+    // one set of loads serves both steps: the header's fields and the first
+    // plane code after them lie within the next 3 (FP32) or 4 (BF16) words
     const uint32_t wi = ql >> 5, sh = ql & 31u;
     const uint32_t x0 = win[wi], x1 = win[wi + 1], x2 = win[wi + 2], x3 = win[wi + 3];
-    const uint32_t v0 = __funnelshift_r(x0, x1, sh), v1 = __funnelshift_r(x1, x2, sh), v2 = __funnelshift_r(x2, x3, sh);
-    f |= v0 & 1u;
-    // header
-    const uint32_t tag = v0 & 7u;
-    const uint32_t n = __popc(__funnelshift_r(v0, v1, 3)) + (W16 ? __popc(__funnelshift_r(v1, v2, 3)) : 0u);
-    const bool masked = (tag == kTagZVC) || (tag == kTagZBX);
-    uint32_t hadv = 3u;
-    hadv += masked ? (W16 ? 64u : 32u) : 0u;
-    hadv += (tag == kTagZVC) ? n * w : 0u;
-    hadv += (tag == kTagDBX) ? w : 0u;
-    hadv += (tag == kTagRAW) ? 1024u : 0u;
-    const bool planes = (tag == kTagBX) || (tag == kTagDBX) || (tag == kTagZBX && n != 0);
-    const int htop = (tag == kTagDBX) ? (int)w : (int)w - 1;
-    const uint32_t hW = (tag == kTagDBX) ? N - 1u : (tag == kTagZBX) ? n : N;
-    // plane codes
-    int m = __ffs(~f) - 1;  // leading verbatim codes, 0..kSkip
-    m = min(m, i + 1);
-    const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4 when not verbatim
-    const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
-    const int rl = (tz == 1u) ? 2 + (int)((v0 >> 2) & ((1u << K) - 1u)) : 1;
-    const bool pbad = (m == 0) && ((rl > i + 1) || (tz == 4u && (v0 & 16u) && i == top));
-    // next state, by selects: a header iteration, a plane iteration, or
-    // none (the lane is done)
-    const bool hdr = i < 0;
-    const bool hrun = run && hdr, prun = run && !hdr;
-    if (hrun && b > 0) rs[b - 1] = (uint16_t)pos;
-    const bool verb = m > 0;
-    const uint32_t padv = verb ? (uint32_t)m * S : len;
-    const int pdec = verb ? m : rl;
-    ok = hrun ? ((tag <= kTagRAW) && pos <= cap) : prun ? !pbad : ok;
-    pos += hrun ? hadv : prun ? padv : 0u;
-    i = hrun ? (planes ? htop : -1) : prun ? i - pdec : i;
-    top = hrun ? htop : top;
-    S = hrun ? 1u + hW : S;
-    pf = hrun ? ceil_log2_u32(hW) : pf;
-    b += hrun ? 1u : 0u;
+    const uint32_t v0 = __funnelshift_r(x0, x1, sh), v1 = __funnelshift_r(x1, x2, sh),
+                   v2 = __funnelshift_r(x2, x3, sh);
+    uint32_t v3 = 0;
+    if (W16) v3 = __funnelshift_r(x3, win[wi + 4], sh);
+    uint32_t off = 0;  // bits from ql to the first plane code of this iteration
+    if (run && i < 0) {  // header step
+      const uint32_t tag = v0 & 7u;
+      uint32_t n = __popc(__funnelshift_r(v0, v1, 3));
+      if (W16) n += __popc(__funnelshift_r(v1, v2, 3));
+      const bool masked = (tag == kTagZVC) || (tag == kTagZBX);
+      uint32_t hadv = 3u;
+      hadv += masked ? N : 0u;
+      hadv += (tag == kTagZVC) ? n * w : 0u;
+      hadv += (tag == kTagDBX) ? w : 0u;
+      hadv += (tag == kTagRAW) ? 1024u : 0u;
+      const bool planes = (tag == kTagBX) || (tag == kTagDBX) || (tag == kTagZBX && n != 0);
+      const uint32_t hW = (tag == kTagDBX) ? N - 1u : (tag == kTagZBX) ? n : N;
+      if (b > 0) rs[b - 1] = (uint16_t)pos;
+      ok = (tag <= kTagRAW) && pos <= cap;
+      pos += hadv;
+      off = hadv;  // 3, 3 + w or 3 + N for a block with plane codes
+      top = (tag == kTagDBX) ? (int)w : (int)w - 1;
+      i = (ok && planes) ? top : -1;
+      S = 1u + hW;
+      pf = ceil_log2_u32(hW);
+      ++b;
+    }
+    if (run && i >= 0) {  // plane step
+      // the 32 bits at ql + off, off in {0, 3, 3 + w, 3 + N}
+      uint32_t c;
+      if (W16)
+        c = (off == 0u) ? v0 : (off == 3u) ? __funnelshift_r(v0, v1, 3) : (off == 3u + w) ? __funnelshift_r(v0, v1, 3u + w)
+                                                                             : __funnelshift_r(v2, v3, 3);
+      else
+        c = (off == 0u) ? v0 : (off == 3u) ? __funnelshift_r(v0, v1, 3) : __funnelshift_r(v1, v2, 3);
+      const bool nv = (c & 1u) == 0u;  // the first code is not verbatim
+      const uint32_t tz = (uint32_t)__ffs(c | 16u) - 1u;  // 1..4 when not verbatim
+      const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
+      const int rl = (tz == 1u) ? 2 + (int)((c >> 2) & ((1u << K) - 1u)) : 1;
+      ok = !(nv && ((rl > i + 1) || (tz == 4u && (c & 16u) && i == top)));
+      const uint32_t len0 = nv ? len : 0u;
+      i -= nv ? rl : 0;
+      // flag k: bit t_k of the window, rotated to position k (the rotations
+      // are independent, and an OR tree joins them)
+      const uint32_t base = ql + off + len0;
+      uint32_t y[kSkip];
+#pragma unroll
+      for (uint32_t k = 0; k < kSkip; ++k) {
+        const uint32_t t = base + k * S;
+        y[k] = __funnelshift_r(win[t >> 5], win[t >> 5], t - k) & (1u << k);
+      }
+      uint32_t f = 0;
+#pragma unroll
+      for (uint32_t k = 0; k < kSkip; k += 2) f |= y[k] | y[k + 1];
+      const int m = min(__ffs(~f) - 1, i + 1);  // leading verbatim codes, 0..kSkip
+      pos += len0 + (uint32_t)max(m, 0) * S;
+      i -= max(m, 0);
+    }
     run = run && ok && (i >= 0 || b < nblk);
   }
   if (!walk) return true;
