@@ -483,25 +483,39 @@ __device__ __forceinline__ void emit_plane(BitWriter &bw, T X, bool prexor_zero,
 // and position codes read the plane. Plane i < 32 (FP32) or < 16 (BF16, low
 // and high 32 symbols in rows i and 16+i) comes from the transposed rows; for
 // DBX the rows hold deltas at bit j = delta index j, so plane bit q = delta
-// q+1 needs a shift, and the top plane (the borrow plane) is passed in topv.
+// q+1 needs a shift. FP32 DBX has a 33rd plane, the borrow plane, on top: it
+// is coded first from its class bits in pl.top and its value topv, so that
+// the loop over planes 31..0 works on 32-bit masks.
 template <bool W16>
 __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase, uint32_t lane, int top,
                                                  int W, int p, bool dbx, uint64_t topv, const Plan &pl) {
   constexpr int K = W16 ? 4 : 5;
-  const bool wide_top = !W16 && dbx;  // FP32 DBX: plane 32 lives in pl.top
-  auto widen = [&](uint32_t m, int k) -> uint64_t {
-    return (uint64_t)m | (wide_top ? ((uint64_t)((pl.top >> k) & 1u) << 32) : 0ull);
-  };
-  const uint64_t NZ = widen(pl.nz, 0), V = widen(pl.v, 1), F5 = widen(pl.f5, 2), FA = widen(pl.fa, 3),
-                 MS = widen(pl.ms, 5);
+  const uint32_t NZ = pl.nz, V = pl.v, F5 = pl.f5, FA = pl.fa, MS = pl.ms;
   const uint32_t lm = 5u + (uint32_t)p;
   int i = top;
+  if (!W16 && dbx) {  // FP32 DBX: plane 32 first
+    if (!(pl.top & 1u)) {  // zero: a run down to the highest non-zero plane below
+      const int hb = NZ ? 31 - __clz((int)NZ) : -1;
+      emit_run(bw, 32 - hb, K);
+      i = hb;
+    } else {
+      if (pl.top & 4u) {
+        bw.put((pl.top & 8u) ? 0u : 16u, 5);  // all ones / pre-XOR plane zero
+      } else if (pl.top & 2u) {
+        bw.put_wide((topv << 1) | 1u, (uint32_t)W + 1);
+      } else {
+        const uint32_t q = (uint32_t)(__ffsll((long long)topv) - 1);
+        bw.put(((pl.top & 32u) ? 24u : 8u) | (q << 5), lm);
+      }
+      i = 31;
+    }
+  }
 #pragma unroll 1
   while (i >= 0) {
-    const uint64_t bit = 1ull << i;
+    const uint32_t bit = 1u << i;
     if (!(NZ & bit)) {  // zero planes i .. hb+1
-      const uint64_t below = NZ & (bit - 1);
-      const int hb = below ? 63 - __clzll((long long)below) : -1;
+      const uint32_t below = NZ & (bit - 1u);
+      const int hb = below ? 31 - __clz((int)below) : -1;
       emit_run(bw, i - hb, K);
       i = hb;
       continue;
@@ -510,7 +524,7 @@ __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase
       bw.put((FA & bit) ? 0u : 16u, 5);  // 0 0 0 0 0 all ones / 0 0 0 0 1 pre-XOR plane zero
     } else {
       uint64_t X;
-      if (dbx && i == top) {
+      if (W16 && dbx && i == top) {
         X = topv;
       } else {
         const uint32_t lo = lds32(plane_row(rowbase, lane, (uint32_t)i));
