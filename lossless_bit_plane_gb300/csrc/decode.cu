@@ -92,8 +92,9 @@ struct StageBits {
 // by selects rather than branches: each plane is
 // X_i, rebuilt to the pre-XOR plane P_i = X_i ^ P_{i+1} and stored in the
 // lane's row (FP32 plane i < 32 in word i; BF16 plane i < 16 in words i and
-// 16+i; DBX rows pre-shifted so row bit j is delta j). One 32x32 bit
-// transpose then turns rows into symbols. Returns false on a malformed code.
+// 16+i; a DBX row's bit j is delta j+1). One 32x32 bit transpose then turns
+// rows into symbols (or deltas, summed afterwards). Returns false on a
+// malformed code.
 template <bool W16>
 __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, uint32_t (&o)[32], uint32_t row,
                                              uint32_t lane) {
@@ -188,9 +189,9 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
           bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
         }
       }
-      const uint32_t Pi = (i == top) ? X : (X ^ Pup);
+      const uint32_t Pi = X ^ Pup;  // Pup is 0 above the top plane
       Pup = Pi;
-      if (i < 32) sts32d(prow(row, lane, (uint32_t)i), dbx ? (Pi << 1) : Pi);
+      if (i < 32) sts32d(prow(row, lane, (uint32_t)i), Pi);
     }
   } else {
     const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
@@ -219,23 +220,27 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
           bad |= (tz == 3u) && (qf + (hi4 ? 0u : 1u) >= (uint32_t)W);
         }
       }
-      const uint64_t Pi = (i == top) ? X : (X ^ Pup);
+      const uint64_t Pi = X ^ Pup;  // Pup is 0 above the top plane
       Pup = Pi;
       if (i < 16) {
-        sts32d(prow(row, lane, (uint32_t)i), dbx ? (uint32_t)(Pi << 1) : (uint32_t)Pi);
-        sts32d(prow(row, lane, (uint32_t)i + 16), dbx ? (uint32_t)(Pi >> 31) : (uint32_t)(Pi >> 32));
+        sts32d(prow(row, lane, (uint32_t)i), (uint32_t)Pi);
+        sts32d(prow(row, lane, (uint32_t)i + 16), (uint32_t)(Pi >> 32));
       }
     }
   }
   const bool ok = !bad;
 #pragma unroll
   for (int j = 0; j < 32; ++j) o[j] = lds32d(prow(row, lane, j));
-  transpose32(o);  // FP32: o[j] = symbol j (or delta j); BF16: split words
+  transpose32(o);  // FP32: o[j] = symbol j (or delta j+1); BF16: split words
   if (!W16) {
-    if (dbx) {
-      o[0] = basesym;
+    if (dbx) {  // s_0 = base, s_j = s_{j-1} + delta j
+      uint32_t prev = basesym;
 #pragma unroll
-      for (int j = 1; j < 32; ++j) o[j] += o[j - 1];
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t d = o[j];
+        o[j] = prev;
+        prev += d;
+      }
     } else if (tag == kTagZBX) {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -248,19 +253,21 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
     }
     return ok;
   }
-  // BF16: o holds split words (word j = symbol j | symbol j+32 << 16)
+  // BF16: o holds split words (word j = symbol j | symbol j+32 << 16); for
+  // DBX, word j holds delta j+1 low and delta j+33 high
   if (dbx) {
     uint32_t prev = basesym;  // s_0
-    o[0] = (o[0] & 0xFFFF0000u) | prev;
 #pragma unroll
-    for (int j = 1; j < 32; ++j) {  // s_j = s_{j-1} + d_j
-      prev = (prev + o[j]) & 0xFFFFu;
+    for (int j = 0; j < 32; ++j) {  // s_j, then s_{j+1} = s_j + delta j+1
+      const uint32_t d = o[j] & 0xFFFFu;
       o[j] = (o[j] & 0xFFFF0000u) | prev;
+      prev = (prev + d) & 0xFFFFu;
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {  // s_{j+32} = s_{j+31} + d_{j+32}
-      prev = (prev + (o[j] >> 16)) & 0xFFFFu;
+    for (int j = 0; j < 32; ++j) {  // s_{j+32}, then s_{j+33} = s_{j+32} + delta j+33
+      const uint32_t d = o[j] >> 16;
       o[j] = (o[j] & 0xFFFFu) | (prev << 16);
+      prev = (prev + d) & 0xFFFFu;
     }
   } else if (tag == kTagZBX) {
     // survivors t_0..t_{W-1}: t_j in o[j] low, t_{j+32} in o[j] high; store
