@@ -270,22 +270,24 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
       prev = (prev + d) & 0xFFFFu;
     }
   } else if (tag == kTagZBX) {
-    // survivors t_0..t_{W-1}: t_j in o[j] low, t_{j+32} in o[j] high; store
-    // them as half-words in index order, then gather each symbol by rank
+    // survivors t_0..t_{W-1}: t_j in o[j] low, t_{j+32} in o[j] high. They
+    // go to the lane's row as half-words in index order (word m = t_2m |
+    // t_2m+1 << 16, the same pairing as a raw word), and each raw word of
+    // the block is gathered from there by its two symbols' ranks.
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < W) sts16d(prow_half(row, lane, j), o[j] & 0xFFFFu);
-      if (j + 32 < W) sts16d(prow_half(row, lane, j + 32), o[j] >> 16);
-    }
+    for (int m = 0; m < 32; ++m) sts32d(prow(row, lane, (uint32_t)m), raw_word_from_split(o, m));
     const uint32_t clo = __popc(mlo);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t rl = __popc(mlo & ((1u << j) - 1u));
-      const uint32_t rh = clo + __popc(mhi & ((1u << j) - 1u));
-      const uint32_t vl = ((mlo >> j) & 1u) ? lds16d(prow_half(row, lane, rl)) : 0u;
-      const uint32_t vh = ((mhi >> j) & 1u) ? lds16d(prow_half(row, lane, rh)) : 0u;
-      o[j] = vl | (vh << 16);
+    for (int r = 0; r < 32; ++r) {  // symbols 2r and 2r + 1
+      const uint32_t m = (r < 16) ? mlo : mhi;
+      const int k = (2 * r) & 31;
+      const uint32_t r0 = ((r < 16) ? 0u : clo) + __popc(m & ((1u << k) - 1u));
+      const uint32_t b0 = (m >> k) & 1u, b1 = (m >> (k + 1)) & 1u;
+      const uint32_t v0 = b0 ? lds16d(prow_half(row, lane, r0)) : 0u;
+      const uint32_t v1 = b1 ? lds16d(prow_half(row, lane, r0 + b0)) : 0u;
+      o[r] = v0 | (v1 << 16);
     }
+    return ok;
   }
   uint32_t sp[32];
 #pragma unroll
