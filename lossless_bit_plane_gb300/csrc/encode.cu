@@ -485,19 +485,27 @@ __device__ __forceinline__ void emit_plane(BitWriter &bw, T X, bool prexor_zero,
 // DBX the rows hold deltas at bit j = delta index j, so plane bit q = delta
 // q+1 needs a shift. FP32 DBX has a 33rd plane, the borrow plane, on top: it
 // is coded first from its class bits in pl.top and its value topv, so that
-// the loop over planes 31..0 works on 32-bit masks.
+// the loop works on 32-bit masks.
+//
+// The loop is plane-major: every lane of the warp stands at the same plane in
+// the same iteration (planes 31..0 for FP32, 16..0 for BF16, where a block
+// without a borrow plane has nothing at 16), so the lanes' branches agree
+// wherever their blocks' planes take the same code, as the low, verbatim
+// planes of activations do. A zero plane emits its run's code at the run's
+// top plane only (RSm); planes above the lane's first uncoded plane were
+// coded already (FP32 DBX) or do not exist.
 template <bool W16>
 __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase, uint32_t lane, int top,
                                                  int W, int p, bool dbx, uint64_t topv, const Plan &pl) {
   constexpr int K = W16 ? 4 : 5;
   const uint32_t NZ = pl.nz, V = pl.v, F5 = pl.f5, FA = pl.fa, MS = pl.ms;
   const uint32_t lm = 5u + (uint32_t)p;
-  int i = top;
+  int first = top;  // the lane's highest plane not yet coded
   if (!W16 && dbx) {  // FP32 DBX: plane 32 first
     if (!(pl.top & 1u)) {  // zero: a run down to the highest non-zero plane below
       const int hb = NZ ? 31 - __clz((int)NZ) : -1;
       emit_run(bw, 32 - hb, K);
-      i = hb;
+      first = hb;
     } else {
       if (pl.top & 4u) {
         bw.put((pl.top & 8u) ? 0u : 16u, 5);  // all ones / pre-XOR plane zero
@@ -507,24 +515,27 @@ __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase
         const uint32_t q = (uint32_t)(__ffsll((long long)topv) - 1);
         bw.put(((pl.top & 32u) ? 24u : 8u) | (q << 5), lm);
       }
-      i = 31;
+      first = 31;
     }
   }
+  const uint32_t Zm = (first < 0) ? 0u : (~NZ & ((2u << first) - 1u));
+  const uint32_t RSm = Zm & ~(Zm >> 1);
 #pragma unroll 1
-  while (i >= 0) {
+  for (int i = W16 ? 16 : 31; i >= 0; --i) {
     const uint32_t bit = 1u << i;
     if (!(NZ & bit)) {  // zero planes i .. hb+1
-      const uint32_t below = NZ & (bit - 1u);
-      const int hb = below ? 31 - __clz((int)below) : -1;
-      emit_run(bw, i - hb, K);
-      i = hb;
+      if (RSm & bit) {
+        const uint32_t below = NZ & (bit - 1u);
+        const int hb = below ? 31 - __clz((int)below) : -1;
+        emit_run(bw, i - hb, K);
+      }
       continue;
     }
     if (F5 & bit) {
       bw.put((FA & bit) ? 0u : 16u, 5);  // 0 0 0 0 0 all ones / 0 0 0 0 1 pre-XOR plane zero
     } else {
       uint64_t X;
-      if (W16 && dbx && i == top) {
+      if (W16 && dbx && i == 16) {
         X = topv;
       } else {
         const uint32_t lo = lds32(plane_row(rowbase, lane, (uint32_t)i));
@@ -547,7 +558,6 @@ __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase
         bw.put(((MS & bit) ? 24u : 8u) | (q << 5), lm);
       }
     }
-    --i;
   }
 }
 
