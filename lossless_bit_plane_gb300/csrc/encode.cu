@@ -765,16 +765,16 @@ __device__ __forceinline__ void copy_out(const uint32_t *buf, uint32_t L, uint8_
 constexpr int kEncWarps = 8;
 constexpr int kOutWords = 1024 + 4;
 
-// Shared memory per warp: kStages 4 KB stage buffers (1024-aligned, the TMA
-// destination), the chunk's output word buffer, two mbarriers. One stage at
-// three CTAs per SM (24 warps): the next chunk is loaded after this one is
-// done, and the other warps cover that load's latency. (Two stages, with the
-// next chunk's load in flight, need more shared memory than three CTAs allow.)
+// Shared memory per warp: one 4 KB stage buffer (1024-aligned, the TMA
+// destination), the chunk's output word buffer, an mbarrier (16 bytes
+// reserved). One stage at three CTAs per SM (24 warps): the next chunk is
+// loaded after this one is done, and the other warps cover that load's
+// latency. (A second stage, with the next chunk's load in flight, needs more
+// shared memory than three CTAs allow.)
 template <bool W16>
 struct EncCfg {
-  static constexpr int kStages = 1;
   static constexpr int kMinCtas = 3;
-  static constexpr size_t kStageBytes = kStages * 4096;
+  static constexpr size_t kStageBytes = 4096;
   static constexpr size_t kOutBytes = kOutWords * 4;
   static constexpr size_t kBytes = 1024 + kEncWarps * kStageBytes + kEncWarps * kOutBytes + kEncWarps * 16;
 };
@@ -797,33 +797,32 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
   const uint32_t warp = threadIdx.x >> 5;
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  uint8_t *stage0 = base + warp * Cfg::kStageBytes;
+  uint8_t *st = base + warp * Cfg::kStageBytes;
   uint32_t *outbuf = reinterpret_cast<uint32_t *>(base + kEncWarps * Cfg::kStageBytes + warp * Cfg::kOutBytes);
   uint64_t *mbar = reinterpret_cast<uint64_t *>(base + kEncWarps * Cfg::kStageBytes + kEncWarps * Cfg::kOutBytes) +
                    2 * warp;
-  const uint32_t mb[2] = {smem_u32(mbar), smem_u32(mbar + 1)};
+  const uint32_t mb = smem_u32(mbar);
   if (lane == 0) {
-    mbar_init(mb[0], 1);
-    mbar_init(mb[1], 1);
+    mbar_init(mb, 1);
     fence_mbar_init();
   }
   __syncwarp();
 
   const uint32_t C = p.num_chunks;
   const uint64_t nbytes = p.nbytes;
-  uint32_t parity[2] = {0, 0};
+  uint32_t parity = 0;
   bool failed = false;
 
   // a chunk is loaded by TMA if its first row lies inside the tensor map
   auto uses_tma = [&](uint32_t t) { return (uint64_t)t * 32u < p.tma_rows; };
-  auto issue = [&](uint32_t t, int sb) {
+  auto issue = [&](uint32_t t) {
     if (lane == 0 && uses_tma(t)) {
-      mbar_arrive_expect_tx(mb[sb], 4096);
-      tma_load_2d(smem_u32(stage0 + sb * 4096), &tmap, 0, (int)(t * 32u), mb[sb]);
+      mbar_arrive_expect_tx(mb, 4096);
+      tma_load_2d(smem_u32(st), &tmap, 0, (int)(t * 32u), mb);
     }
   };
   // plain loads for bytes that the tensor map does not cover
-  auto patch = [&](uint32_t t, uint8_t *st) {
+  auto patch = [&](uint32_t t) {
     const uint64_t c0 = (uint64_t)t * 4096u;
     const uint32_t raw_len = (uint32_t)umin64(4096u, nbytes - c0);
     uint32_t from = 0;
@@ -853,20 +852,15 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
   unsigned long long size_sum = 0;  // sizes only: this warp's sum of 2 + L
 
   uint32_t u = kSizeOnly ? warp_id : next_unit(0);
-  int cur = 0;
-  if (u < U) issue(chunk_of(u), cur);
+  if (u < U) issue(chunk_of(u));
 
   while (u < U) {
     const uint32_t t = chunk_of(u);
-    const uint32_t nu = next_unit(u);
-    if (Cfg::kStages == 2 && nu < U) issue(chunk_of(nu), cur ^ 1);  // prefetch the next chunk
-
-    uint8_t *st = stage0 + cur * 4096;
     if (uses_tma(t)) {
-      if (!mbar_wait(mb[cur], parity[cur], kMbarPollLimit)) failed = true;
-      parity[cur] ^= 1u;
+      if (!mbar_wait(mb, parity, kMbarPollLimit)) failed = true;
+      parity ^= 1u;
     }
-    patch(t, st);
+    patch(t);
 
     const uint64_t c0 = (uint64_t)t * 4096u;
     const uint32_t raw_len = (uint32_t)umin64(4096u, nbytes - c0);
@@ -898,8 +892,8 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
       }
       __syncwarp();
       fence_proxy_async_smem();  // generic-proxy use of the stage before the next TMA write
-      u = nu;
-      if (u < U) issue(chunk_of(u), cur);
+      u = next_unit(u);
+      if (u < U) issue(chunk_of(u));
       continue;
     }
     if (lane == 0) st_relaxed_u64(p.status + t, (t == 0 ? kFlagInc : kFlagAgg) | L);
@@ -938,11 +932,11 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
 
     __syncwarp();
     fence_proxy_async_smem();  // generic-proxy use of the stage before the next TMA write
-    u = nu;
-    if (Cfg::kStages == 2)
-      cur ^= 1;
-    else if (u < U)
-      issue(chunk_of(u), cur);  // one stage: load the next chunk now that this one is done
+    // The next ticket is taken only now: a warp that holds a ticket is always
+    // working toward that chunk's size, so no look-back waits on a chunk whose
+    // warp is still busy with its previous one.
+    u = next_unit(u);
+    if (u < U) issue(chunk_of(u));  // one stage: load the next chunk now that this one is done
   }
   if (kSizeOnly && lane == 0 && size_sum) atomicAdd(p.total, size_sum);
   if (failed && lane == 0) atomicMax(p.total, ~0ull);
