@@ -56,11 +56,14 @@ __device__ __forceinline__ void sts16d(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
 }
 // Lane-private 32-word row, XOR-swizzled by lane (conflict-free across lanes).
-__device__ __forceinline__ uint32_t prow(uint32_t row, uint32_t lane, uint32_t word) {
-  return row + (((word ^ lane) & 31u) << 2);
+// The row starts on a 128-byte boundary (the tile is 128-aligned), so the
+// swizzled word offset can be XORed into the row's address: the
+// lane-dependent part is common to every access of the lane.
+__device__ __forceinline__ uint32_t prow(uint32_t row, uint32_t lane, uint32_t word) {  // word, lane < 32
+  return (row ^ (lane << 2)) ^ (word << 2);
 }
-__device__ __forceinline__ uint32_t prow_half(uint32_t row, uint32_t lane, uint32_t h) {
-  return prow(row, lane, h >> 1) + ((h & 1u) << 1);
+__device__ __forceinline__ uint32_t prow_half(uint32_t row, uint32_t lane, uint32_t h) {  // h < 64
+  return (row ^ (lane << 2)) ^ (h << 1);
 }
 
 // A chunk's payload staged in shared memory: word k holds stream bytes
@@ -814,7 +817,7 @@ __device__ __forceinline__ uint32_t tile_swz(uint32_t r, uint32_t u) { return r 
 template <bool W16>
 __global__ void __launch_bounds__(kDecWarps * 32, 3)
     decode_kernel(DecodeArgs p) {
-  __shared__ __align__(16) uint32_t tile[kDecWarps][32 * 32];  // per warp: 32 lane rows of 128 B
+  __shared__ __align__(128) uint32_t tile[kDecWarps][32 * 32];  // per warp: 32 lane rows of 128 B
   __shared__ __align__(16) uint32_t stage[kDecWarps][kStageWords];  // per warp: the chunk's payload
   __shared__ uint16_t tail_starts[kDecWarps][32];
   const uint32_t lane = lane_id();

@@ -146,11 +146,17 @@ __device__ __forceinline__ void keep_smallest(Sizes &z, const Plan &bx, const Pl
 
 // The lane's block in its 128-byte row of the stage, as the TMA left it
 // (16-byte units swizzled by row): unit u holds words 4u .. 4u+3.
-__device__ __forceinline__ uint4 stage_unit(uint32_t rowbase, uint32_t r, uint32_t u) {
+// Row addresses: a lane's 128-byte row of the stage starts on a 128-byte
+// boundary (the stage is 1024-aligned), so a byte offset below 128, however
+// swizzled, can be XORed into the row's address instead of added; the
+// lane-dependent part of the swizzle (row_swz) is then common to every
+// access and the per-access cost is one shift and one XOR.
+__device__ __forceinline__ uint32_t row_swz(uint32_t rowbase, uint32_t r) { return rowbase ^ ((r & 7u) << 4); }
+__device__ __forceinline__ uint4 stage_unit(uint32_t rowbase, uint32_t r, uint32_t u) {  // u < 8
   uint4 q;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
-               : "r"(rowbase + ((u ^ (r & 7u)) << 4))
+               : "r"(row_swz(rowbase, r) ^ (u << 4))
                : "memory");
   return q;
 }
@@ -417,14 +423,14 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
 // transposed plane rows (XOR-swizzled by lane). Per-plane work runs as short
 // runtime loops over that row so that the kernel's code stays small.
 
-__device__ __forceinline__ uint32_t stage_word(uint32_t rowbase, uint32_t r, uint32_t k) {
-  return rowbase + ((((k >> 2) ^ (r & 7u)) << 4) | ((k & 3u) << 2));
+__device__ __forceinline__ uint32_t stage_word(uint32_t rowbase, uint32_t r, uint32_t k) {  // k < 32
+  return row_swz(rowbase, r) ^ (k << 2);
 }
-__device__ __forceinline__ uint32_t stage_half(uint32_t rowbase, uint32_t r, uint32_t h) {
-  return stage_word(rowbase, r, h >> 1) + ((h & 1u) << 1);
+__device__ __forceinline__ uint32_t stage_half(uint32_t rowbase, uint32_t r, uint32_t h) {  // h < 64
+  return row_swz(rowbase, r) ^ (h << 1);
 }
-__device__ __forceinline__ uint32_t plane_row(uint32_t rowbase, uint32_t lane, uint32_t i) {
-  return rowbase + (((i ^ lane) & 31u) << 2);
+__device__ __forceinline__ uint32_t plane_row(uint32_t rowbase, uint32_t lane, uint32_t i) {  // i, lane < 32
+  return (rowbase ^ (lane << 2)) ^ (i << 2);
 }
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
