@@ -194,7 +194,7 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
       }
       const uint32_t Pi = X ^ Pup;  // Pup is 0 above the top plane
       Pup = Pi;
-      if (i < 32) sts32d(prow(row, lane, (uint32_t)i), Pi);
+      if (i < 32) sts32d(row + ((((uint32_t)i ^ lane) & 31u) << 2), Pi);  // prow(row, lane, i), added (faster here)
     }
   } else {
     const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
