@@ -943,6 +943,13 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     // warp is still busy with its previous one.
     u = next_unit(u);
     if (u < U) issue(chunk_of(u));  // one stage: load the next chunk now that this one is done
+    // The chunk one wave of tickets ahead (every warp of the grid takes one
+    // ticket per wave) is brought into L2, so that its warp's TMA load finds
+    // it there; each chunk is prefetched once, by the warp one wave before.
+    if (lane == 0 && (uint64_t)(u + nwarps + 1) * 32u <= p.tma_rows)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.in + (uint64_t)(u + nwarps) * 4096u),
+                   "r"(4096u)
+                   : "memory");
   }
   if (kSizeOnly && lane == 0 && size_sum) atomicAdd(p.total, size_sum);
   if (failed && lane == 0) atomicMax(p.total, ~0ull);
