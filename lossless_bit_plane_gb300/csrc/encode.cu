@@ -125,6 +125,7 @@ struct Sizes {
   uint32_t m0, m1;  // non-zero symbol masks: symbols 0..31 and (BF16) 32..63
   uint32_t tag, bits;  // the kept candidate and its size (tag excluded)
   Plan win;            // its plan (plane candidates only)
+  uint64_t bp;         // DBX's borrow plane (bit q = borrow of delta q+1)
 };
 
 // Pick the smallest allowed candidate (bit t of cand = tag t; the raw block
@@ -265,6 +266,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
     const uint64_t Z = (uint64_t)(uint32_t)~ad | ((uint64_t)(Bw == 0) << 32);
     z.s[kTagDBX] = 32 + run_cost(Z, 5) + plan_cost(dbx, 31, 5) + plan_cost(tp, 31, 5);
   }
+  z.bp = Bw;
   keep_smallest(z, bx, zbx, dbx, cand);
   return z;
 }
@@ -405,6 +407,7 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     const uint32_t andd16 = lo(andd) & hi(andd);
     const uint32_t ord16 = lo(ord) | hi(ord);
     const uint64_t Bp = (uint64_t)Blo | ((uint64_t)Bhi << 32);
+    z.bp = Bp;
     const int bones = __popcll(Bp);
     const uint32_t tnz = (Bp != 0), tA = (Bp == (1ull << 63) - 1), tS = (bones == 1),
                    tT = (bones == 2) && ((Bp & (Bp >> 1)) != 0);
@@ -569,7 +572,7 @@ __device__ __forceinline__ void emit_plane_codes(BitWriter &bw, uint32_t rowbase
 
 // FP32 emit of the chosen candidate. s: the block's symbols; nz: non-zero mask.
 __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t nz, uint32_t rowbase, uint32_t lane,
-                                      const Plan &pl) {
+                                      const Plan &pl, uint64_t bp) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -594,26 +597,27 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t nz,
       const uint32_t t = ((uint32_t)j < cnt) ? lds32(stage_word(rowbase, lane, j)) : 0u;
       T[j] = t ^ (t >> 1);
     }
-  } else if (tag == kTagDBX) {
-    uint32_t s[32];
-    load_block<false>(rowbase, lane, s);
-    bw.put(s[0], 32);
-    uint32_t Bw = 0;
-    T[0] = 0;
-#pragma unroll
-    for (int j = 1; j < 32; ++j) {
-      const uint64_t d = (uint64_t)s[j] - (uint64_t)s[j - 1];
-      const uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);
-      Bw |= hi & (1u << (j - 1));
-      T[j] = lo ^ __funnelshift_r(lo, hi, 1);
-    }
-    topv = Bw;
-    top = 32;
-    W = 31;
   } else {
-    load_block<false>(rowbase, lane, T);
+    load_block<false>(rowbase, lane, T);  // BX and DBX
+    if (tag == kTagDBX) {  // deltas (33 bits: bit 32 is the borrow), Gray-coded; the borrow plane came from classify
+      bw.put(T[0], 32);
+      uint32_t prev = T[0];
+      T[0] = 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) T[j] ^= T[j] >> 1;
+      for (int j = 1; j < 32; ++j) {
+        const uint32_t cur = T[j];
+        const uint64_t d = (uint64_t)cur - (uint64_t)prev;
+        const uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);
+        T[j] = lo ^ __funnelshift_r(lo, hi, 1);
+        prev = cur;
+      }
+      topv = bp;
+      top = 32;
+      W = 31;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) T[j] ^= T[j] >> 1;
+    }
   }
   transpose32(T);
 #pragma unroll
@@ -624,7 +628,7 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t nz,
 // BF16 emit of the chosen candidate. sp: split-packed symbols (word j =
 // symbol j | symbol j+32 << 16); mlo/mhi: non-zero masks of 0..31 / 32..63.
 __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t mlo, uint32_t mhi, uint32_t rowbase,
-                                      uint32_t lane, const Plan &pl) {
+                                      uint32_t lane, const Plan &pl, uint64_t bp) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) bw.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -660,33 +664,30 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t mlo
       const uint32_t t = split_word(rw, j) & keep;
       T[j] = t ^ ((t >> 1) & 0x7FFF7FFFu);
     }
-  } else if (tag == kTagDBX) {
-    uint32_t sp[32];
-    load_block<true>(rowbase, lane, sp);
-    bw.put(sp[0] & 0xFFFFu, 16);
-    const uint32_t s31lo = sp[31] << 16;
-    uint32_t Blo = 0, Bhi = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      uint32_t bo;
-      uint32_t d = sub16x2(sp[j], j ? sp[j - 1] : s31lo, bo);
-      if (j == 0) {
-        d &= 0xFFFF0000u;
-        bo &= 0x80000000u;
-        Blo |= bo;
-      } else {
-        Blo |= ((bo >> 15) & 1u) << (j - 1);
-        Bhi |= (bo >> 31) << (j - 1);
-      }
-      T[j] = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
-    }
-    topv = (uint64_t)Blo | ((uint64_t)Bhi << 32);
-    top = 16;
-    W = 63;
   } else {
-    load_block<true>(rowbase, lane, T);
+    load_block<true>(rowbase, lane, T);  // BX and DBX
+    if (tag == kTagDBX) {  // deltas (17 bits: bit 16 is the borrow), Gray-coded; the borrow plane came from classify
+      bw.put(T[0] & 0xFFFFu, 16);
+      uint32_t prev = T[31] << 16;  // word 0: no delta for s_0 (the base); d_32 = s_32 - s_31
 #pragma unroll
-    for (int j = 0; j < 32; ++j) T[j] ^= (T[j] >> 1) & 0x7FFF7FFFu;
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t cur = T[j];
+        uint32_t bo;
+        uint32_t d = sub16x2(cur, prev, bo);
+        if (j == 0) {
+          d &= 0xFFFF0000u;
+          bo &= 0x80000000u;
+        }
+        T[j] = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
+        prev = cur;
+      }
+      topv = bp;
+      top = 16;
+      W = 63;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) T[j] ^= (T[j] >> 1) & 0x7FFF7FFFu;
+    }
   }
   transpose32(T);
 #pragma unroll
@@ -914,9 +915,9 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
         bw.put(tag, 3);
         const Plan &pl = z.win;
         if (W16)
-          emit16(bw, tag, z.m0, z.m1, rowbase, lane, pl);
+          emit16(bw, tag, z.m0, z.m1, rowbase, lane, pl, z.bp);
         else
-          emit32(bw, tag, z.m0, rowbase, lane, pl);
+          emit32(bw, tag, z.m0, rowbase, lane, pl, z.bp);
         bw.flush();
       }
     } else {
