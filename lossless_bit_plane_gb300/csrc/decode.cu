@@ -512,11 +512,10 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
   constexpr uint32_t N = W16 ? 64u : 32u;   // symbols per block
   constexpr uint32_t K = W16 ? 4u : 5u;     // run field
   constexpr uint32_t kSkip = W16 ? 6u : 10u;  // BF16 blocks have at most 7 verbatim planes in a row
-  // bits an iteration may read past its position: four (FP32) or five
-  // (BF16) words at the position, or a plane block's header fields (tag and
-  // mask, or tag and base), one code of at most 11 bits and kSkip flags
-  // N + 1 apart
-  constexpr uint32_t kPlaneReach = 3u + N + 11u + (kSkip - 1u) * (N + 1u) + 64u;
+  // bits an iteration may read past its position: five words at the
+  // position, or a plane block's header fields (tag and mask, or tag and
+  // base), two codes of at most 11 bits each and kSkip flags N + 1 apart
+  constexpr uint32_t kPlaneReach = 3u + N + 22u + (kSkip - 1u) * (N + 1u) + 64u;
   constexpr uint32_t kAhead = (kPlaneReach > 160u ? kPlaneReach : 160u) + 32u;
   const uint32_t lane = lane_id();
   const uint64_t a0 = off & ~15ull;
@@ -563,14 +562,18 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
     // walking lane re-based its window above), and keeps every read inside
     const uint32_t ql = min(qa - wbase, kWinUnits * 128u - kAhead);
     // one set of loads serves both steps: the header's fields and the first
-    // plane code after them lie within the next 3 (FP32) or 4 (BF16) words
+    // two plane codes after them lie within the 128 bits at the position
     const uint32_t wi = ql >> 5, sh = ql & 31u;
-    const uint32_t x0 = win[wi], x1 = win[wi + 1], x2 = win[wi + 2], x3 = win[wi + 3];
+    const uint32_t x0 = win[wi], x1 = win[wi + 1], x2 = win[wi + 2], x3 = win[wi + 3], x4 = win[wi + 4];
     const uint32_t v0 = __funnelshift_r(x0, x1, sh), v1 = __funnelshift_r(x1, x2, sh),
-                   v2 = __funnelshift_r(x2, x3, sh);
-    uint32_t v3 = 0;
-    if (W16) v3 = __funnelshift_r(x3, win[wi + 4], sh);
-    uint32_t off = 0;  // bits from ql to the first plane code of this iteration
+                   v2 = __funnelshift_r(x2, x3, sh), v3 = __funnelshift_r(x3, x4, sh);
+    // the 32 bits at ql + o, o < 96
+    auto bits_at = [&](uint32_t o) -> uint32_t {
+      const uint32_t wq = o >> 5;
+      const uint32_t a = (wq == 0u) ? v0 : (wq == 1u) ? v1 : v2, c = (wq == 0u) ? v1 : (wq == 1u) ? v2 : v3;
+      return __funnelshift_r(a, c, o & 31u);
+    };
+    uint32_t offb = 0;  // bits from ql to the first plane code of this iteration
     if (run && i < 0) {  // header step
       const uint32_t tag = v0 & 7u;
       uint32_t n = __popc(__funnelshift_r(v0, v1, 3));
@@ -586,7 +589,7 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
       if (b > 0) rs[b - 1] = (uint16_t)pos;
       ok = (tag <= kTagRAW) && pos <= cap;
       pos += hadv;
-      off = hadv;  // 3, 3 + w or 3 + N for a block with plane codes
+      offb = hadv;  // 3, 3 + w or 3 + N for a block with plane codes
       top = (tag == kTagDBX) ? (int)w : (int)w - 1;
       i = (ok && planes) ? top : -1;
       S = 1u + hW;
@@ -594,23 +597,28 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
       ++b;
     }
     if (run && i >= 0) {  // plane step
-      // the 32 bits at ql + off, off in {0, 3, 3 + w, 3 + N}
-      uint32_t c;
-      if (W16)
-        c = (off == 0u) ? v0 : (off == 3u) ? __funnelshift_r(v0, v1, 3) : (off == 3u + w) ? __funnelshift_r(v0, v1, 3u + w)
-                                                                             : __funnelshift_r(v2, v3, 3);
-      else
-        c = (off == 0u) ? v0 : (off == 3u) ? __funnelshift_r(v0, v1, 3) : __funnelshift_r(v1, v2, 3);
-      const bool nv = (c & 1u) == 0u;  // the first code is not verbatim
-      const uint32_t tz = (uint32_t)__ffs(c | 16u) - 1u;  // 1..4 when not verbatim
-      const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
-      const int rl = (tz == 1u) ? 2 + (int)((c >> 2) & ((1u << K) - 1u)) : 1;
-      ok = !(nv && ((rl > i + 1) || (tz == 4u && (c & 16u) && i == top)));
-      const uint32_t len0 = nv ? len : 0u;
-      i -= nv ? rl : 0;
+      // up to two codes that are not verbatim, each classified by its leading
+      // zeros; the second is parsed only after a first and while planes remain
+      const uint32_t c1 = bits_at(offb);
+      const bool nv1 = (c1 & 1u) == 0u;
+      const uint32_t tz1 = (uint32_t)__ffs(c1 | 16u) - 1u;  // 1..4 when not verbatim
+      const uint32_t len1 = (tz1 == 1u) ? 2u + K : (tz1 == 2u) ? 3u : (tz1 == 3u) ? 5u + pf : 5u;
+      const int rl1 = (tz1 == 1u) ? 2 + (int)((c1 >> 2) & ((1u << K) - 1u)) : 1;
+      bool bad = nv1 && ((rl1 > i + 1) || (tz1 == 4u && (c1 & 16u) && i == top));
+      const uint32_t o2 = offb + (nv1 ? len1 : 0u);
+      i -= nv1 ? rl1 : 0;
+      const uint32_t c2 = bits_at(o2);
+      const bool nv2 = nv1 && (c2 & 1u) == 0u && i >= 0;  // below the top plane: no pre-XOR-zero check
+      const uint32_t tz2 = (uint32_t)__ffs(c2 | 16u) - 1u;
+      const uint32_t len2 = (tz2 == 1u) ? 2u + K : (tz2 == 2u) ? 3u : (tz2 == 3u) ? 5u + pf : 5u;
+      const int rl2 = (tz2 == 1u) ? 2 + (int)((c2 >> 2) & ((1u << K) - 1u)) : 1;
+      bad = bad || (nv2 && rl2 > i + 1);
+      const uint32_t o3 = o2 + (nv2 ? len2 : 0u);
+      i -= nv2 ? rl2 : 0;
+      ok = !bad;
       // flag k: bit t_k of the window, rotated to position k (the rotations
       // are independent, and an OR tree joins them)
-      const uint32_t base = ql + off + len0;
+      const uint32_t base = ql + o3;
       uint32_t y[kSkip];
 #pragma unroll
       for (uint32_t k = 0; k < kSkip; ++k) {
@@ -621,7 +629,7 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
 #pragma unroll
       for (uint32_t k = 0; k < kSkip; k += 2) f |= y[k] | y[k + 1];
       const int m = min(__ffs(~f) - 1, i + 1);  // leading verbatim codes, 0..kSkip
-      pos += len0 + (uint32_t)max(m, 0) * S;
+      pos += (o3 - offb) + (uint32_t)max(m, 0) * S;
       i -= max(m, 0);
     }
     run = run && ok && (i >= 0 || b < nblk);
