@@ -112,27 +112,33 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
     return true;
   }
   if (tag == kTagZVC) {
+    // the non-zero symbols follow the mask back to back, w bits each: the
+    // symbol k is read straight from its rank's position (no serial walk)
     if (W16) {
       const uint32_t mlo = sb.peek32(q), mhi = sb.peek32(q + 32);
       q += 64;
-#pragma unroll 1
-      for (uint32_t h = 0; h < 64; ++h) {
-        const uint32_t bit = ((h < 32) ? (mlo >> h) : (mhi >> (h - 32))) & 1u;
-        sts16d(prow_half(row, lane, h), bit ? (sb.peek32(q) & 0xFFFFu) : 0u);
-        q += bit * 16u;
+      const uint32_t clo = __popc(mlo);
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {  // raw word r: symbols 2r and 2r + 1
+        const uint32_t m = (r < 16) ? mlo : mhi;
+        const int k = (2 * r) & 31;
+        const uint32_t r0 = ((r < 16) ? 0u : clo) + __popc(m & ((1u << k) - 1u));
+        const uint32_t b0 = (m >> k) & 1u, b1 = (m >> (k + 1)) & 1u;
+        const uint32_t v0 = b0 ? (sb.peek32(q + 16u * r0) & 0xFFFFu) : 0u;
+        const uint32_t v1 = b1 ? (sb.peek32(q + 16u * (r0 + b0)) & 0xFFFFu) : 0u;
+        o[r] = v0 | (v1 << 16);
       }
+      q += 16u * (clo + __popc(mhi));
     } else {
       const uint32_t mask = sb.peek32(q);
       q += 32;
-#pragma unroll 1
-      for (uint32_t k = 0; k < 32; ++k) {
-        const uint32_t bit = (mask >> k) & 1u;
-        sts32d(prow(row, lane, k), bit ? sb.peek32(q) : 0u);
-        q += bit * 32u;
-      }
-    }
 #pragma unroll
-    for (int k = 0; k < 32; ++k) o[k] = lds32d(prow(row, lane, k));
+      for (int k = 0; k < 32; ++k) {
+        const uint32_t rk = __popc(mask & ((1u << k) - 1u));
+        o[k] = ((mask >> k) & 1u) ? sb.peek32(q + 32u * rk) : 0u;
+      }
+      q += 32u * __popc(mask);
+    }
     return true;
   }
   uint32_t basesym = 0, mlo = 0, mhi = 0;
