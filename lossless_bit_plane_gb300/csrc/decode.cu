@@ -78,13 +78,6 @@ struct StageBits {
     const uint32_t a = addr(q);
     return __funnelshift_r(lds32d(a), lds32d(a + 4), q & 31u);
   }
-  // bits [q, q + 64) and bit q + 64
-  __device__ __forceinline__ uint64_t peek64(uint32_t q, uint32_t &bit64) const {
-    const uint32_t a = addr(q), sh = q & 31u;
-    const uint32_t w0 = lds32d(a), w1 = lds32d(a + 4), w2 = lds32d(a + 8);
-    bit64 = (w2 >> sh) & 1u;
-    return (uint64_t)__funnelshift_r(w0, w1, sh) | ((uint64_t)__funnelshift_r(w1, w2, sh) << 32);
-  }
 };
 
 // Decode the block whose tag is at stage bit q into o[32] (the block's 32
@@ -204,6 +197,7 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
     }
   } else {
     const uint64_t full = (W >= 64) ? ~0ull : ((1ull << W) - 1);
+    const uint32_t full_lo = (uint32_t)full, full_hi = (uint32_t)(full >> 32);
     uint64_t Pup = 0;
 #pragma unroll 1
     for (int i = top; i >= 0; --i) {
@@ -211,11 +205,12 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
       if (run > 0) {
         --run;
       } else {
-        uint32_t b64;
-        const uint64_t win = sb.peek64(q, b64);
-        const uint32_t lo = (uint32_t)win;
-        if (lo & 1u) {  // verbatim: 1 + the plane
-          X = (W >= 64) ? ((win >> 1) | ((uint64_t)b64 << 63)) : ((win >> 1) & full);
+        const uint32_t a = sb.addr(q), sh = q & 31u;
+        const uint32_t w0 = lds32d(a), w1 = lds32d(a + 4), w2 = lds32d(a + 8);
+        const uint32_t lo = __funnelshift_r(w0, w1, sh), hi = __funnelshift_r(w1, w2, sh);
+        if (lo & 1u) {  // verbatim: 1 + the plane (bits 1..64 after the flag)
+          const uint32_t xl = __funnelshift_r(lo, hi, 1) & full_lo, xh = __funnelshift_r(hi, w2 >> sh, 1) & full_hi;
+          X = (uint64_t)xl | ((uint64_t)xh << 32);
           q += 1u + (uint32_t)W;
         } else {
           const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // 1..4
