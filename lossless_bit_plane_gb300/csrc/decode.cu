@@ -173,11 +173,13 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
       if (run > 0) {
         --run;
       } else {
+        // a code spans at most 33 bits (1 + W, W <= 32), so the two words
+        // under q hold it: bit q + 32 is bit sh of w1
         const uint32_t a = sb.addr(q), sh = q & 31u;
-        const uint32_t w0 = lds32d(a), w1 = lds32d(a + 4), w2 = lds32d(a + 8);
-        const uint32_t lo = __funnelshift_r(w0, w1, sh), hi = __funnelshift_r(w1, w2, sh);
+        const uint32_t w0 = lds32d(a), w1 = lds32d(a + 4);
+        const uint32_t lo = __funnelshift_r(w0, w1, sh);
         if (lo & 1u) {  // verbatim: 1 + the plane
-          X = __funnelshift_r(lo, hi, 1) & full;
+          X = __funnelshift_r(lo, w1 >> sh, 1) & full;
           q += 1u + (uint32_t)W;
         } else {
           const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // 1..4
