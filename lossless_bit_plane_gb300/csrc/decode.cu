@@ -480,8 +480,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
 }
 
 // Walk kernel shape: warps of 32 chunks (lane = chunk); each lane reads its
-// chunk through a window of kWinUnits 16-byte units in shared memory.
-constexpr uint32_t kWalkWarps = 2;
+// chunk through a window of kWinUnits 16-byte units in shared memory. One
+// warp per CTA spreads the warps evenly over the SMs (6 or 7 per SM for a
+// 128 MiB input rather than 3 or 4 CTAs of two), and the kernel lasts as long
+// as its slowest warp.
+constexpr uint32_t kWalkWarps = 1;
 constexpr uint32_t kWinUnits = 48;
 constexpr uint32_t kWinWords = kWinUnits * 4;
 // windows are laid out kWinStride words apart (4 words more than a window,
