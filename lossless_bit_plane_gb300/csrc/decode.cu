@@ -6,26 +6,32 @@
 // chunk sizes and decodes chunks in parallel; each block is the inverse of
 // its tagged candidate (Section III-A "Codec").
 //
-// GPU design:
+// GPU design (up to three launches per call):
 //  - The format stores no per-block offsets: block b of a chunk starts where
-//    block b-1 ends, so a chunk's blocks must be parsed in order. Parallelism
-//    therefore comes from chunks: LANE = CHUNK. A warp decodes 32 chunks at
-//    once, each lane walking its own chunk's 32 blocks in sequence, so the
-//    serial prefix-code parse runs SIMD across 32 chunks.
-//  - Chunk offsets: each CTA sums all headers before its first chunk
-//    (16-byte vector loads, L2-resident, reduced in shared memory) and scans
-//    its own 128 headers; no scratch memory and no inter-CTA waiting.
-//  - Raw chunks (L == raw size) are copied by the whole warp with coalesced
-//    16-byte stores; compressed chunks are parsed by their lane through an
-//    LSB-first bit reader over read-only cached 32-bit loads with one word
-//    of look-ahead.
-//  - Planes are rebuilt top-down in registers (pre-XOR plane P_i = X_i ^
-//    P_{i+1}), turned back into symbols by one 32x32 bit transpose, then the
-//    delta is undone (prefix sum) or the survivors are scattered back (ZBX)
-//    through a lane-private shared-memory scratch.
+//    block b-1 ends, so a chunk's blocks must be measured in order before
+//    they can be decoded in parallel. A walk finds every block's start bit;
+//    a decode kernel then decodes the blocks, LANE = BLOCK.
+//  - Chunk offsets: a small kernel sums the 16-bit sizes of each group of
+//    2048 chunks; a walk warp adds the group sums before its group and the
+//    sizes of its own group's earlier chunks.
+//  - Walk, above 8192 chunks: LANE = CHUNK, one warp per CTA. Each lane
+//    measures its chunk's codes through a window in shared memory, refilled
+//    warp-wide by bulk copies; a step takes a block header and up to two
+//    non-verbatim codes and skips a run of verbatim codes by testing their
+//    flag bits. Up to 8192 chunks: WARP = CHUNK, the 32 lanes testing 32
+//    flags at once (shorter chains for small inputs).
+//  - Records: a chunk's payload offset and its blocks' start bits go into
+//    the first 72 bytes of the chunk's own output region; the decode warp
+//    reads them before it overwrites those bytes.
+//  - Decode: WARP = CHUNK, LANE = BLOCK. The payload is staged in shared
+//    memory; each lane rebuilds its planes top-down (pre-XOR plane P_i =
+//    X_i ^ P_{i+1}) into a lane-private row, one 32x32 bit transpose turns
+//    them into symbols, then the delta is undone (prefix sum) or the
+//    survivors are scattered back by rank (ZBX); ZVC symbols are read by
+//    rank. Raw chunks are copied by the whole warp with 16-byte stores.
 //  - Every field is validated; a malformed chunk sets PZ_ERR_CORRUPT in the
-//    status word and stops; no write leaves the chunk's output range and no
-//    read leaves the input.
+//    status word; no write leaves the chunk's output range and no read
+//    leaves the 16-byte granules of the input.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -37,7 +43,7 @@
 namespace pz {
 
 constexpr int kDecWarps = 8;
-constexpr uint32_t kStageWords = (4096 + 16) / 4 + 4;  // 257 16-byte units + slack for 64-bit peeks
+constexpr uint32_t kStageWords = (4096 + 16) / 4 + 4;  // 257 16-byte units + slack for three-word peeks
 
 __device__ __forceinline__ uint32_t lds32d(uint32_t addr) {
   uint32_t v;
@@ -339,13 +345,12 @@ struct WindowPeeker {  // adapts WindowReader to the ensure / peek_resident inte
   __device__ __forceinline__ uint32_t peek(uint32_t pos) const { return r.peek(pos); }
 };
 
-// Walk one chunk: record each block's start bit (relative to the chunk)
-// through put_start(b, pos) and check that the chunk is exactly
-// ceil(bits/8) bytes with zero padding.
+// Walk one chunk by one thread: record each block's start bit (relative to
+// the chunk) through put_start(b, pos) and check that the chunk is exactly
+// ceil(bits/8) bytes with zero padding. The decode kernel uses it for a final
+// chunk too short (under 72 bytes) to hold a walk record.
 //
-// The walk is one flat loop whose body is the same instruction stream for
-// every lane (selects, not branches), so that 32 lanes walking 32 chunks
-// stay converged however their blocks differ. An iteration either reads a
+// An iteration either reads a
 // block header (tag; the mask of ZVC / ZBX; the base of DBX) and skips what
 // needs no parsing, or advances over plane codes: it tests the flag bits of
 // the next eight codes under the assumption that they are verbatim (1 + W

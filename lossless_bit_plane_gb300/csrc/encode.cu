@@ -8,13 +8,15 @@
 // stored raw); Section II-B (BPC's Delta-BitPlane-XOR).
 //
 // GPU design (one kernel does load, classify, select, emit, scan, scatter):
-//  - Persistent warps take chunks in ticket order (atomic counter). A warp
-//    owns a 4 KB chunk; LANE b OWNS BLOCK b and works on it alone, so the
-//    per-block work is SIMD over 32 blocks rather than cooperative.
+//  - Persistent warps take chunks in ticket order (atomic counter), the next
+//    ticket only once the current chunk is done. A warp owns a 4 KB chunk;
+//    LANE b OWNS BLOCK b and works on it alone, so the per-block work is SIMD
+//    over 32 blocks rather than cooperative.
 //  - The chunk arrives by a 2D TMA tile load (32 rows x 128 B, 128-byte
-//    swizzle) into a double-buffered shared stage; the next chunk's load is
-//    in flight while the current one is coded. The swizzle makes each lane's
-//    row read (8 x 16 B) bank-conflict free.
+//    swizzle) into the warp's shared stage; the other warps of the SM cover
+//    its latency, and each warp prefetches into L2 the chunk one wave of
+//    tickets ahead. The swizzle makes each lane's row read (8 x 16 B)
+//    bank-conflict free.
 //  - Candidate sizes come from plane CLASSES, computed bit-sliced over the
 //    32 words a lane holds: the XOR of adjacent planes is the Gray code
 //    g = v ^ (v >> 1) of each symbol, and per-plane "any one", "two or more",
@@ -24,7 +26,8 @@
 //  - Only the winning candidate is materialised: its planes come from one
 //    32x32 bit transpose in registers, and its codes go into a shared chunk
 //    buffer through an LSB-first writer at the block's bit offset (a warp
-//    prefix sum over the lanes' block sizes).
+//    prefix sum over the lanes' block sizes), plane by plane with every lane
+//    of the warp at the same plane.
 //  - Chunk offsets come from a single-pass decoupled look-back over 8-byte
 //    status words (flag | value) in the scratch tail of the output buffer,
 //    with a bounded spin; the warp then copies its chunk to its final byte
