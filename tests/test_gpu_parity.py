@@ -214,6 +214,39 @@ def test_corrupt_streams_report_status_above_the_cooperative_walk_size():
             assert out[4096 * c: 4096 * c + piece.size] == out_ref
 
 
+@pytest.mark.parametrize("dtype,seg_mib", [("fp32", 36), ("bf16", 34)])
+def test_corrupt_attention_streams_above_the_cooperative_walk_size(dtype, seg_mib):
+    # Causal-attention data codes most blocks as DBX or BX with several short
+    # (non-verbatim) plane codes per block, which the thread walk parses up to
+    # two at a time; 9,216 / 8,704 chunks take that walk. One bit is flipped
+    # per call, in the last rows' chunks (the longest code sequences), and the
+    # oracle judges the flipped chunk on its own.
+    t = W.sweep_segment("attention", dtype, seed=31, seg_bytes=seg_mib << 20)
+    ew = t.elem_width
+    data = t.data
+    n = data.size
+    s = bytearray(oracle.compress(data, ew))
+    lens, offs = chunk_table(bytes(s), n)
+    C = lens.size
+    assert C > 8192
+    st, back = gpu_decompress(bytes(s), n, ew)
+    assert st == 0 and back == data.tobytes()
+    rng = np.random.default_rng(37)
+    for _ in range(32):
+        c = int(rng.integers(C - 256, C))
+        L = int(lens[c])
+        bad = bytearray(s)
+        bit = int(rng.integers(0, 8 * L))
+        bad[offs[c] + bit // 8] ^= 1 << (bit % 8)
+        st, out = gpu_decompress(bytes(bad), n, ew)
+        piece = data[4096 * c: 4096 * c + 4096]
+        mini = int(L).to_bytes(2, "little") + bytes(bad[offs[c]: offs[c] + L])
+        rc_ref, out_ref = oracle.decompress_status(mini, piece.size, ew)
+        assert st == rc_ref, (c, bit)
+        if st == 0:
+            assert out[4096 * c: 4096 * c + piece.size] == out_ref
+
+
 def test_repeated_calls_and_streams_are_deterministic():
     t = W.relu_fp32_4mib()
     x = to_device(t.data)
