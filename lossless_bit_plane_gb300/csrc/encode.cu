@@ -595,13 +595,9 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t nz,
     for (uint32_t m = nz; m; m &= m - 1, ++cnt)
       sts32(stage_word(rowbase, lane, cnt), lds32(stage_word(rowbase, lane, __ffs(m) - 1)));
     W = (int)cnt;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t t = ((uint32_t)j < cnt) ? lds32(stage_word(rowbase, lane, j)) : 0u;
-      T[j] = t ^ (t >> 1);
-    }
-  } else {
-    load_block<false>(rowbase, lane, T);  // BX and DBX
+  }
+  {
+    load_block<false>(rowbase, lane, T);  // BX, DBX and the compacted ZBX row
     if (tag == kTagDBX) {  // deltas (33 bits: bit 32 is the borrow), Gray-coded; the borrow plane came from classify
       bw.put(T[0], 32);
       uint32_t prev = T[0];
@@ -617,9 +613,12 @@ __device__ __forceinline__ void emit32(BitWriter &bw, uint32_t tag, uint32_t nz,
       topv = bp;
       top = 32;
       W = 31;
-    } else {
+    } else {  // BX, or ZBX over its first W (compacted) words
 #pragma unroll
-      for (int j = 0; j < 32; ++j) T[j] ^= T[j] >> 1;
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t t = (j < W) ? T[j] : 0u;
+        T[j] = t ^ (t >> 1);
+      }
     }
   }
   transpose32(T);
@@ -657,18 +656,9 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t mlo
       sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, 31 + __ffs(m))));
     if (cnt == 0) return;
     W = (int)cnt;
-    uint32_t rw[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) rw[r] = lds32(stage_word(rowbase, lane, r));
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t keep =
-          (((uint32_t)j < cnt) ? 0x0000FFFFu : 0u) | (((uint32_t)j + 32 < cnt) ? 0xFFFF0000u : 0u);
-      const uint32_t t = split_word(rw, j) & keep;
-      T[j] = t ^ ((t >> 1) & 0x7FFF7FFFu);
-    }
-  } else {
-    load_block<true>(rowbase, lane, T);  // BX and DBX
+  }
+  {
+    load_block<true>(rowbase, lane, T);  // BX, DBX and the compacted ZBX row
     if (tag == kTagDBX) {  // deltas (17 bits: bit 16 is the borrow), Gray-coded; the borrow plane came from classify
       bw.put(T[0] & 0xFFFFu, 16);
       uint32_t prev = T[31] << 16;  // word 0: no delta for s_0 (the base); d_32 = s_32 - s_31
@@ -687,9 +677,13 @@ __device__ __forceinline__ void emit16(BitWriter &bw, uint32_t tag, uint32_t mlo
       topv = bp;
       top = 16;
       W = 63;
-    } else {
+    } else {  // BX, or ZBX over its first W (compacted) half-words
 #pragma unroll
-      for (int j = 0; j < 32; ++j) T[j] ^= (T[j] >> 1) & 0x7FFF7FFFu;
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t keep = ((j < W) ? 0x0000FFFFu : 0u) | ((j + 32 < W) ? 0xFFFF0000u : 0u);
+        const uint32_t t = T[j] & keep;
+        T[j] = t ^ ((t >> 1) & 0x7FFF7FFFu);
+      }
     }
   }
   transpose32(T);
