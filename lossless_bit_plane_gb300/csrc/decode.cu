@@ -504,13 +504,14 @@ constexpr uint32_t kWalkSmem = kWalkWarps * 32 * kWinStride * 4 + kWalkWarps * 8
 //  - a header step, when the lane stands at a block: the tag, the mask of
 //    ZVC / ZBX or the base of DBX; what needs no parsing (ZVC symbols, a
 //    raw block) is skipped, and a block with plane codes goes on to
-//  - a plane step in the same iteration: at most one code that is not
-//    verbatim, classified by its leading zero bits (stream order, capped at
-//    4): 01 run (2+K bits, 2+field planes), 001 single zero (3), 0001x
-//    position code (5+p), 0000x all-ones / pre-XOR-zero (5); then the flag
-//    bits of the next kSkip codes are tested under the assumption that they
-//    are verbatim (1 + W bits each) and the m leading verbatim ones are
-//    skipped.
+//  - a plane step in the same iteration: up to two codes that are not
+//    verbatim, each classified by its leading zero bits (stream order,
+//    capped at 4): 01 run (2+K bits, 2+field planes), 001 single zero (3),
+//    0001x position code (5+p), 0000x all-ones / pre-XOR-zero (5); then the
+//    flag bits of the next kSkip codes are tested under the assumption that
+//    they are verbatim (1 + W bits each) and the m leading verbatim ones are
+//    skipped. The header fields and the first two codes are read from the
+//    same five words loaded at the position.
 // A lane's window holds the units from the one under its position on; when
 // any lane's next iteration could read past its window, every walking lane
 // re-bases its window at its position with one bulk copy, and the warp waits
