@@ -823,6 +823,21 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
       }
       pos += len;
       i -= rl;
+      // a second non-verbatim code in the same step: the 32 bits at the old
+      // position hold it too (each code is at most 11 bits); below the top
+      // plane, so only its run length needs checking
+      const uint32_t v1 = v0 >> len;
+      if (i >= 0 && (v1 & 1u) == 0u) {
+        const uint32_t tz2 = (uint32_t)__ffs(v1 | 16u) - 1u;
+        const uint32_t len2 = (tz2 == 1u) ? 2u + K : (tz2 == 2u) ? 3u : (tz2 == 3u) ? 5u + pf : 5u;
+        const int rl2 = (tz2 == 1u) ? 2 + (int)((v1 >> 2) & ((1u << K) - 1u)) : 1;
+        if (rl2 > i + 1) {
+          ok = false;
+          break;
+        }
+        pos += len2;
+        i -= rl2;
+      }
     }
     if (pos > cap) ok = false;
   }
