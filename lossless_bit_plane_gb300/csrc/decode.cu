@@ -707,8 +707,10 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
 // shared memory by one bulk copy, the warp steps through the blocks with
 // every value warp-uniform, and lane k tests the flag bit of the k-th code
 // ahead under the assumption that the codes are verbatim (1 + W bits each),
-// so one ballot skips up to 32 verbatim planes. It writes the same record
-// as the walk kernel (offset and block starts at the chunk's output region).
+// so one ballot skips up to 32 verbatim planes; a step that stands at a code
+// that is not verbatim parses up to four such codes in a row from 64 bits.
+// It writes the same record as the walk kernel (offset and block starts at
+// the chunk's output region).
 
 constexpr uint32_t kCoopWarps = 8;
 constexpr uint32_t kCoopStageBytes = 4096 + 32;  // a payload from its 16-byte unit, plus slack
@@ -814,30 +816,26 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
         i -= m;
         continue;
       }
-      const uint32_t tz = (uint32_t)__ffs(v0 | 16u) - 1u;  // 1..4: the code is not verbatim
-      const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
-      const int rl = (tz == 1u) ? 2 + (int)((v0 >> 2) & ((1u << K) - 1u)) : 1;
-      if (rl > i + 1 || (tz == 4u && (v0 & 16u) && i == top)) {
-        ok = false;
-        break;
-      }
-      pos += len;
-      i -= rl;
-      // a second non-verbatim code in the same step: the 32 bits at the old
-      // position hold it too (each code is at most 11 bits); below the top
-      // plane, so only its run length needs checking
-      const uint32_t v1 = v0 >> len;
-      if (i >= 0 && (v1 & 1u) == 0u) {
-        const uint32_t tz2 = (uint32_t)__ffs(v1 | 16u) - 1u;
-        const uint32_t len2 = (tz2 == 1u) ? 2u + K : (tz2 == 2u) ? 3u : (tz2 == 3u) ? 5u + pf : 5u;
-        const int rl2 = (tz2 == 1u) ? 2 + (int)((v1 >> 2) & ((1u << K) - 1u)) : 1;
-        if (rl2 > i + 1) {
+      // the code at pos is not verbatim: up to four such codes in a row are
+      // parsed from the 64 bits at pos (each is at most 11 bits); only the
+      // first can stand at the top plane
+      uint64_t v = (uint64_t)v0 | ((uint64_t)peek(pos + 32u) << 32);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = (uint32_t)v;
+        if (k > 0 && (i < 0 || (lo & 1u))) break;  // a verbatim code, or no planes left
+        const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // 1..4
+        const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
+        const int rl = (tz == 1u) ? 2 + (int)((lo >> 2) & ((1u << K) - 1u)) : 1;
+        if (rl > i + 1 || (tz == 4u && (lo & 16u) && i == top)) {
           ok = false;
           break;
         }
-        pos += len2;
-        i -= rl2;
+        pos += len;
+        i -= rl;
+        v >>= len;
       }
+      if (!ok) break;
     }
     if (pos > cap) ok = false;
   }
