@@ -14,11 +14,11 @@
 //  - Chunk offsets: a small kernel sums the 16-bit sizes of each group of
 //    2048 chunks; a walk warp adds the group sums before its group and the
 //    sizes of its own group's earlier chunks.
-//  - Walk, above 8192 chunks: LANE = CHUNK, one warp per CTA. Each lane
+//  - Walk, above 6144 chunks: LANE = CHUNK, one warp per CTA. Each lane
 //    measures its chunk's codes through a window in shared memory, refilled
 //    warp-wide by bulk copies; a step takes a block header and up to two
 //    non-verbatim codes and skips a run of verbatim codes by testing their
-//    flag bits. Up to 8192 chunks: WARP = CHUNK, the 32 lanes testing 32
+//    flag bits. Up to 6144 chunks: WARP = CHUNK, the 32 lanes testing 32
 //    flags at once (shorter chains for small inputs).
 //  - Records: a chunk's payload offset and its blocks' start bits go into
 //    the first 72 bytes of the chunk's own output region; the decode warp
@@ -716,7 +716,7 @@ constexpr uint32_t kCoopWarps = 8;
 constexpr uint32_t kCoopStageBytes = 4096 + 32;  // a payload from its 16-byte unit, plus slack
 constexpr uint32_t kCoopStageWords = kCoopStageBytes / 4;
 constexpr uint32_t kCoopSmem = kCoopWarps * kCoopStageBytes + kCoopWarps * 8;
-constexpr uint32_t kCoopMaxChunks = 8192;
+constexpr uint32_t kCoopMaxChunks = 6144;
 
 // Sum of the sizes of chunks [0, c) for any c, by a warp (group sums of
 // whole groups, then 16-byte units of headers, then the last few headers).

@@ -186,9 +186,35 @@ def test_corrupt_streams_report_status():
             assert out == out_ref
 
 
+@pytest.mark.parametrize("dtype,ew", [("fp32", 4), ("bf16", 2)])
+def test_corrupt_attention_streams_on_the_cooperative_walk(dtype, ew):
+    # 1,024 / 512 chunks of causal attention (DBX and BX blocks with runs of
+    # short codes, parsed several per step by the cooperative warp walk): one
+    # random bit flipped per call anywhere past the size table, judged by the
+    # oracle on the whole stream.
+    t = W.sweep_segment("attention", dtype, seed=41, seg_bytes=(4 if dtype == "fp32" else 2) << 20)
+    data = t.data.tobytes()
+    n = len(data)
+    s = bytearray(oracle.compress(data, ew))
+    C = (n + 4095) // 4096
+    assert C <= 6144
+    st, back = gpu_decompress(bytes(s), n, ew)
+    assert st == 0 and back == data
+    rng = np.random.default_rng(43)
+    for _ in range(64):
+        bad = bytearray(s)
+        pos = int(rng.integers(16 * C, len(bad) * 8))
+        bad[pos // 8] ^= 1 << (pos % 8)
+        st, out = gpu_decompress(bytes(bad), n, ew)
+        rc_ref, out_ref = oracle.decompress_status(bytes(bad), n, ew)
+        assert st == rc_ref, pos
+        if st == 0:
+            assert out == out_ref
+
+
 def test_corrupt_streams_report_status_above_the_cooperative_walk_size():
     # 8,500 chunks: decompress walks chunks one thread each (inputs of up to
-    # 8,192 chunks take the cooperative warp walk, covered above). Bits are
+    # 6,144 chunks take the cooperative warp walk, covered above). Bits are
     # flipped in the payloads of the last chunks only; since chunks are
     # independent, the oracle judges each flip on that chunk alone.
     rng = np.random.default_rng(29)
@@ -228,7 +254,7 @@ def test_corrupt_attention_streams_above_the_cooperative_walk_size(dtype, seg_mi
     s = bytearray(oracle.compress(data, ew))
     lens, offs = chunk_table(bytes(s), n)
     C = lens.size
-    assert C > 8192
+    assert C > 6144
     st, back = gpu_decompress(bytes(s), n, ew)
     assert st == 0 and back == data.tobytes()
     rng = np.random.default_rng(37)
