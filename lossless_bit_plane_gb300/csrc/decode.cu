@@ -705,10 +705,12 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
 // by one thread's chain through a whole chunk, whatever the input's size.
 // Here a warp walks one chunk instead: the chunk's payload is staged in
 // shared memory by one bulk copy, the warp steps through the blocks with
-// every value warp-uniform, and lane k tests the flag bit of the k-th code
-// ahead under the assumption that the codes are verbatim (1 + W bits each),
-// so one ballot skips up to 32 verbatim planes; a step that stands at a code
-// that is not verbatim parses up to four such codes in a row from 64 bits.
+// every value warp-uniform. In a step lane k loads the 64 bits at the k-th
+// code ahead under the assumption that the codes are verbatim (1 + W bits
+// each), so one ballot of their flag bits skips up to 32 verbatim planes;
+// the lane that stands at the first code that is not verbatim hands its 64
+// bits to the warp, which parses up to four such codes in a row from them in
+// the same step.
 // It writes the same record as the walk kernel (offset and block starts at
 // the chunk's output region).
 
@@ -805,29 +807,33 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     int i = planes ? top : -1;
 #pragma unroll 1
     while (i >= 0) {
-      const uint32_t q = bit0 + pos + lane * S;
-      const uint32_t fw = word(q >> 5);
-      const uint32_t v0 = peek(pos);  // loaded with the flags: one round of loads per step
-      const uint32_t f = __ballot_sync(0xFFFFFFFFu, (fw >> (q & 31u)) & 1u);
-      int m = (f == 0xFFFFFFFFu) ? 32 : __ffs(~f) - 1;  // leading verbatim codes
-      m = min(m, i + 1);
-      if (m > 0) {
-        pos += (uint32_t)m * S;
-        i -= m;
-        continue;
+      // lane k holds the 64 bits at the k-th code ahead, were the codes
+      // before it verbatim; its lowest bit is that code's flag
+      const uint32_t q = bit0 + pos + lane * S, qi = q >> 5;
+      const uint32_t x0 = word(qi), x1 = word(qi + 1), x2 = word(qi + 2);
+      const uint32_t lo = __funnelshift_r(x0, x1, q & 31u), hi = __funnelshift_r(x1, x2, q & 31u);
+      const uint32_t f = __ballot_sync(0xFFFFFFFFu, lo & 1u);
+      const int m = (f == 0xFFFFFFFFu) ? 32 : __ffs(~f) - 1;  // leading verbatim codes
+      if (m > i) {  // the block's remaining planes are all verbatim
+        pos += (uint32_t)(i + 1) * S;
+        break;
       }
-      // the code at pos is not verbatim: up to four such codes in a row are
-      // parsed from the 64 bits at pos (each is at most 11 bits); only the
-      // first can stand at the top plane
-      uint64_t v = (uint64_t)v0 | ((uint64_t)peek(pos + 32u) << 32);
+      pos += (uint32_t)m * S;
+      i -= m;
+      if (m == 32) continue;  // FP32 DBX: a 33rd plane remains
+      // the code after the m verbatim ones is not verbatim: lane m holds the
+      // 64 bits at it, from which up to four such codes in a row are parsed
+      // (each is at most 11 bits); only a first code with m = 0 can stand at
+      // the top plane
+      uint64_t v = (uint64_t)__shfl_sync(0xFFFFFFFFu, lo, m) | ((uint64_t)__shfl_sync(0xFFFFFFFFu, hi, m) << 32);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t lo = (uint32_t)v;
-        if (k > 0 && (i < 0 || (lo & 1u))) break;  // a verbatim code, or no planes left
-        const uint32_t tz = (uint32_t)__ffs(lo | 16u) - 1u;  // 1..4
+        const uint32_t cw = (uint32_t)v;
+        if (k > 0 && (i < 0 || (cw & 1u))) break;  // a verbatim code, or no planes left
+        const uint32_t tz = (uint32_t)__ffs(cw | 16u) - 1u;  // 1..4
         const uint32_t len = (tz == 1u) ? 2u + K : (tz == 2u) ? 3u : (tz == 3u) ? 5u + pf : 5u;
-        const int rl = (tz == 1u) ? 2 + (int)((lo >> 2) & ((1u << K) - 1u)) : 1;
-        if (rl > i + 1 || (tz == 4u && (lo & 16u) && i == top)) {
+        const int rl = (tz == 1u) ? 2 + (int)((cw >> 2) & ((1u << K) - 1u)) : 1;
+        if (rl > i + 1 || (tz == 4u && (cw & 16u) && i == top)) {
           ok = false;
           break;
         }
