@@ -29,6 +29,7 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   int enc_ctas_per_sm[4] = {0, 0, 0, 0};  // [2 * size_only + w16]
+  size_t fused_max_chunks[2] = {0, 0};   // [w16]: one resident wave of the fused walk and decode
 };
 
 std::mutex g_mu;
@@ -62,6 +63,13 @@ cudaError_t device_info(DeviceInfo &out) {
       if ((e = cudaFuncSetAttribute(pz::walk_kernel_ptr(w == 1), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)pz::walk_smem_bytes())) != cudaSuccess)
         return e;
+    for (int w = 0; w < 2; ++w) {
+      int n = 0;
+      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pz::walk_decode_kernel_ptr(w == 1),
+                                                             32 * pz::fused_warps(), 0)) != cudaSuccess)
+        return e;
+      d.fused_max_chunks[w] = (size_t)n * (size_t)d.sms * (size_t)pz::fused_warps();
+    }
     if (!g_encode_tiled) {
       void *fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -246,6 +254,13 @@ pz_status pz::decompress_launch(const void *d_in, size_t comp_bytes, int elem_wi
   if (groups > 1 && cudaLaunchKernel(pz::size_sum_kernel_ptr(), dim3((unsigned)(groups - 1)), dim3(256), args, 0,
                                      s) != cudaSuccess)
     return PZ_ERR_CUDA;
+  if (C <= info.fused_max_chunks[w16 ? 1 : 0]) {  // one resident wave: a warp walks and decodes each chunk
+    const size_t fw = (size_t)pz::fused_warps();
+    if (cudaLaunchKernel(pz::walk_decode_kernel_ptr(w16), dim3((unsigned)((C + fw - 1) / fw)),
+                         dim3((unsigned)(32 * fw)), args, 0, s) != cudaSuccess)
+      return PZ_ERR_CUDA;
+    return PZ_OK;
+  }
   if (C <= pz::coop_max_chunks()) {  // small input: a warp walks each chunk
     const size_t cw = (size_t)pz::coop_warps();
     if (cudaLaunchKernel(pz::walk_coop_kernel_ptr(w16), dim3((unsigned)((C + cw - 1) / cw)), dim3((unsigned)(32 * cw)),

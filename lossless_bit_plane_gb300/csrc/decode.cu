@@ -734,48 +734,17 @@ __device__ __forceinline__ unsigned long long sizes_before_chunk(const DecodeArg
   return warp_sum_u64(part);
 }
 
-template <bool W16>
-__global__ void __launch_bounds__(kCoopWarps * 32)
-    walk_coop_kernel(DecodeArgs p) {
+// The warp's walk of one staged chunk (WARP = CHUNK, every value
+// warp-uniform): stage word k holds payload bytes from 4k on, the payload
+// starting at stage bit bit0; rec(b, pos) is called with the start bit of
+// each block b >= 1 (relative to bit0). Returns false where the chunk is
+// malformed.
+template <bool W16, typename Rec>
+__device__ __forceinline__ bool coop_walk(const uint32_t *stage, uint32_t bit0, uint32_t L, uint32_t nblk,
+                                          uint32_t lane, Rec rec) {
   constexpr uint32_t w = W16 ? 16u : 32u;   // bits per symbol = BX planes
   constexpr uint32_t N = W16 ? 64u : 32u;   // symbols per block
   constexpr uint32_t K = W16 ? 4u : 5u;     // run field
-  extern __shared__ __align__(128) uint8_t coop_smem[];
-  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-  const uint32_t C = p.num_chunks;
-  const uint32_t c = blockIdx.x * kCoopWarps + warp;
-  if (c >= C) return;
-  const uint32_t *stage = reinterpret_cast<const uint32_t *>(coop_smem + warp * kCoopStageBytes);
-  const uint32_t mb = smem_u32(coop_smem + kCoopWarps * kCoopStageBytes) + warp * 8u;
-  const uint64_t off = 2ull * C + sizes_before_chunk(p, c, lane);
-  const uint32_t L = __ldg(reinterpret_cast<const uint16_t *>(p.in) + c);
-  const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
-  if (L == 0 || L > raw_len || off + L > p.comp_bytes) {
-    if (lane == 0) atomicMax(p.status, kErrCorrupt);
-    return;
-  }
-  if (raw_len < kRecordBytes) return;  // the decode warp handles it
-  uint8_t *rec = p.out + (uint64_t)c * 4096u;
-  if (lane == 0) *reinterpret_cast<unsigned long long *>(rec) = off;
-  if (L == raw_len) return;  // raw chunk: the offset is all the decoder needs
-
-  const uint64_t a0 = off & ~15ull;
-  const uint32_t bytes = (uint32_t)(((off + L + 15) & ~15ull) - a0);  // <= 4112
-  if (lane == 0) {
-    mbar_init(mb, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  if (lane == 0) {
-    mbar_arrive_expect_tx(mb, bytes);
-    bulk_load(smem_u32(stage), p.in + a0, bytes, mb);
-  }
-  if (!__all_sync(0xFFFFFFFFu, mbar_wait(mb, 0, kMbarPolls))) {
-    mbar_wait(mb, 0, kMbarPolls);  // leave no copy in flight
-    if (lane == 0) atomicMax(p.status, kErrTimeout);
-    return;
-  }
-  const uint32_t bit0 = (uint32_t)(off - a0) * 8u;
   // word indices are clamped to the stage: a malformed stream cannot read
   // outside it (valid streams never reach the clamp)
   auto word = [&](uint32_t i) { return stage[min(i, kCoopStageWords - 1u)]; };
@@ -784,13 +753,11 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
     return __funnelshift_r(word(i), word(i + 1), q & 31u);
   };
   const uint32_t cap = 8u * L;
-  const uint32_t nblk = (raw_len + 127u) >> 7;
-  uint16_t *rs = reinterpret_cast<uint16_t *>(rec + 8);  // start of block b at rs[b - 1]
   uint32_t pos = 0;
   bool ok = true;
 #pragma unroll 1
   for (uint32_t b = 0; b < nblk && ok; ++b) {
-    if (b && lane == 0) rs[b - 1] = (uint16_t)pos;
+    if (b) rec(b, pos);
     const uint32_t tag = peek(pos) & 7u;
     if (tag > kTagRAW) {
       ok = false;
@@ -847,11 +814,155 @@ __global__ void __launch_bounds__(kCoopWarps * 32)
   }
   if (ok && cap - pos >= 8) ok = false;
   if (ok && cap > pos && (peek(pos) & ((1u << (cap - pos)) - 1u))) ok = false;
+  return ok;
+}
+
+template <bool W16>
+__global__ void __launch_bounds__(kCoopWarps * 32)
+    walk_coop_kernel(DecodeArgs p) {
+  extern __shared__ __align__(128) uint8_t coop_smem[];
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t C = p.num_chunks;
+  const uint32_t c = blockIdx.x * kCoopWarps + warp;
+  if (c >= C) return;
+  const uint32_t *stage = reinterpret_cast<const uint32_t *>(coop_smem + warp * kCoopStageBytes);
+  const uint32_t mb = smem_u32(coop_smem + kCoopWarps * kCoopStageBytes) + warp * 8u;
+  const uint64_t off = 2ull * C + sizes_before_chunk(p, c, lane);
+  const uint32_t L = __ldg(reinterpret_cast<const uint16_t *>(p.in) + c);
+  const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
+  if (L == 0 || L > raw_len || off + L > p.comp_bytes) {
+    if (lane == 0) atomicMax(p.status, kErrCorrupt);
+    return;
+  }
+  if (raw_len < kRecordBytes) return;  // the decode warp handles it
+  uint8_t *rec = p.out + (uint64_t)c * 4096u;
+  if (lane == 0) *reinterpret_cast<unsigned long long *>(rec) = off;
+  if (L == raw_len) return;  // raw chunk: the offset is all the decoder needs
+
+  const uint64_t a0 = off & ~15ull;
+  const uint32_t bytes = (uint32_t)(((off + L + 15) & ~15ull) - a0);  // <= 4112
+  if (lane == 0) {
+    mbar_init(mb, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive_expect_tx(mb, bytes);
+    bulk_load(smem_u32(stage), p.in + a0, bytes, mb);
+  }
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait(mb, 0, kMbarPolls))) {
+    mbar_wait(mb, 0, kMbarPolls);  // leave no copy in flight
+    if (lane == 0) atomicMax(p.status, kErrTimeout);
+    return;
+  }
+  const uint32_t bit0 = (uint32_t)(off - a0) * 8u;
+  uint16_t *rs = reinterpret_cast<uint16_t *>(rec + 8);  // start of block b at rs[b - 1]
+  const bool ok = coop_walk<W16>(stage, bit0, L, (raw_len + 127u) >> 7, lane, [rs, lane](uint32_t b, uint32_t pos) {
+    if (lane == 0) rs[b - 1] = (uint16_t)pos;
+  });
   if (!ok && lane == 0) atomicMax(p.status, kErrCorrupt);
 }
 
 // Byte offset of 16-byte unit u of row r in a 128-byte-swizzled 4 KB tile.
 __device__ __forceinline__ uint32_t tile_swz(uint32_t r, uint32_t u) { return r * 128u + ((u ^ (r & 7u)) << 4); }
+
+// A raw chunk: the warp copies raw_len bytes from stream byte off (any
+// alignment) to dst.
+__device__ __forceinline__ void copy_raw_chunk(const uint8_t *in, uint64_t off, uint32_t raw_len, uint8_t *dst,
+                                               uint32_t lane) {
+  // output unit v comes from aligned source units v and v+1 (16-byte
+  // loads), realigned by the chunk's byte offset within a unit, which is
+  // the same for the whole warp
+  const uint64_t a0 = off & ~15ull;
+  const uint32_t s = (uint32_t)(off - a0);
+  const uint32_t nunits = (uint32_t)((((off + raw_len + 15) & ~15ull) - a0) >> 4);
+  const uint4 *src = reinterpret_cast<const uint4 *>(in + a0);
+  const uint32_t ws = s >> 2, bs = (s & 3u) * 8u;
+  // a lane's loads are issued four units at a time (eight 16-byte loads in
+  // flight), so that enough bytes are in flight to cover the memory latency
+  constexpr int kR = 4;
+#pragma unroll 1
+  for (uint32_t v0 = lane; v0 * 16 < raw_len; v0 += 32u * kR) {
+    uint4 As[kR], Bs[kR];
+#pragma unroll
+    for (int i = 0; i < kR; ++i) {
+      const uint32_t v = v0 + 32u * i;
+      As[i] = (v < nunits) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+      Bs[i] = (v + 1 < nunits) ? __ldg(src + v + 1) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kR; ++i) {
+      const uint32_t v = v0 + 32u * i;
+      if (v * 16 >= raw_len) break;
+      const uint4 A = As[i], B = Bs[i];
+      const uint32_t a[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+      uint32_t o[4];
+      switch (ws) {  // the same for every lane
+        case 0:
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k], a[k + 1], bs);
+          break;
+        case 1:
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 1], a[k + 2], bs);
+          break;
+        case 2:
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 2], a[k + 3], bs);
+          break;
+        default:
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 3], a[k + 4], bs);
+          break;
+      }
+      if (v * 16 + 16 <= raw_len) {
+        *reinterpret_cast<uint4 *>(dst + 16ull * v) = make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+        for (uint32_t b = 0; v * 16 + b < raw_len; ++b) dst[16ull * v + b] = (uint8_t)(o[b >> 2] >> ((b & 3) * 8));
+      }
+    }
+  }
+}
+
+// Decode a staged chunk: lane b < nblk decodes block b, whose code starts at
+// stage bit bit0 + s0 (the next block's at bit0 + s1), into its row of the
+// warp's tile; the warp then writes the chunk's raw_len bytes to dst with
+// coalesced 16-byte stores. Returns false in a lane whose block is malformed.
+template <bool W16>
+__device__ __forceinline__ bool decode_staged(uint32_t sbase, uint32_t bit0, uint32_t s0, uint32_t s1, uint32_t nblk,
+                                              uint32_t L, uint32_t raw_len, uint32_t *tw, uint8_t *dst,
+                                              uint32_t lane) {
+  const StageBits sb{sbase};
+  bool ok = true;
+  const uint32_t row = smem_u32(tw) + lane * 128u;
+  if (lane < nblk) {
+    uint32_t q = bit0 + s0;
+    uint32_t o[32];
+    ok = decode_block<W16>(sb, q, o, row, lane);
+    const uint32_t used = q - bit0 - s0;
+    if (lane + 1 < nblk && used != s1 - s0) ok = false;
+    if (lane + 1 == nblk && s0 + used > 8u * L) ok = false;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(tw) + tile_swz(lane, u)) =
+          make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+  }
+  __syncwarp();
+  // coalesced write-out of the chunk
+#pragma unroll
+  for (uint32_t i = 0; i < 8; ++i) {
+    const uint32_t v = lane + 32u * i;
+    if (16u * v >= raw_len) break;
+    const uint4 q = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(tw) + tile_swz(v >> 3, v & 7));
+    if (16u * v + 16u <= raw_len) {
+      *reinterpret_cast<uint4 *>(dst + 16u * v) = q;
+    } else {
+      const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+      for (uint32_t b = 0; 16u * v + b < raw_len; ++b) dst[16u * v + b] = (uint8_t)(qq[b >> 2] >> ((b & 3) * 8));
+    }
+  }
+  return ok;
+}
 
 template <bool W16>
 __global__ void __launch_bounds__(kDecWarps * 32, 3)
@@ -908,58 +1019,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
   __syncwarp();  // every lane has read the record before any output is written
 
   if (L == raw_len) {  // raw chunk: the warp copies it (source at any byte offset)
-    // output unit v comes from aligned source units v and v+1 (16-byte
-    // loads), realigned by the chunk's byte offset within a unit, which is
-    // the same for the whole warp
-    const uint64_t a0 = off & ~15ull;
-    const uint32_t s = (uint32_t)(off - a0);
-    const uint32_t nunits = (uint32_t)((((off + raw_len + 15) & ~15ull) - a0) >> 4);
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.in + a0);
-    const uint32_t ws = s >> 2, bs = (s & 3u) * 8u;
-    // a lane's loads are issued four units at a time (eight 16-byte loads in
-    // flight), so that enough bytes are in flight to cover the memory latency
-    constexpr int kR = 4;
-#pragma unroll 1
-    for (uint32_t v0 = lane; v0 * 16 < raw_len; v0 += 32u * kR) {
-      uint4 As[kR], Bs[kR];
-#pragma unroll
-      for (int i = 0; i < kR; ++i) {
-        const uint32_t v = v0 + 32u * i;
-        As[i] = (v < nunits) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-        Bs[i] = (v + 1 < nunits) ? __ldg(src + v + 1) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int i = 0; i < kR; ++i) {
-        const uint32_t v = v0 + 32u * i;
-        if (v * 16 >= raw_len) break;
-        const uint4 A = As[i], B = Bs[i];
-        const uint32_t a[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
-        uint32_t o[4];
-        switch (ws) {  // the same for every lane
-          case 0:
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k], a[k + 1], bs);
-            break;
-          case 1:
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 1], a[k + 2], bs);
-            break;
-          case 2:
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 2], a[k + 3], bs);
-            break;
-          default:
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(a[k + 3], a[k + 4], bs);
-            break;
-        }
-        if (v * 16 + 16 <= raw_len) {
-          *reinterpret_cast<uint4 *>(dst + 16ull * v) = make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-          for (uint32_t b = 0; v * 16 + b < raw_len; ++b) dst[16ull * v + b] = (uint8_t)(o[b >> 2] >> ((b & 3) * 8));
-        }
-      }
-    }
+    copy_raw_chunk(p.in, off, raw_len, dst, lane);
     return;
   }
 
@@ -980,41 +1040,82 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
     }
   }
   __syncwarp();
-  const StageBits sb{sbase};
   const uint32_t bit0 = (uint32_t)(off - a0) * 8u;
+  if (!decode_staged<W16>(sbase, bit0, s0, s1, nblk, L, raw_len, tile[warp], dst, lane)) atomicMax(p.status, kErrCorrupt);
+}
 
-  uint32_t *tw = tile[warp];
-  const uint32_t row = smem_u32(tw) + lane * 128u;
-  if (lane < nblk) {
-    uint32_t q = bit0 + s0;
-    uint32_t o[32];
-    ok = decode_block<W16>(sb, q, o, row, lane);
-    const uint32_t used = q - bit0 - s0;
-    if (lane + 1 < nblk && used != s1 - s0) ok = false;
-    if (lane + 1 == nblk && s0 + used > 8u * L) ok = false;
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(tw) + tile_swz(lane, u)) =
-          make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+// ------------------------------------------- fused walk and decode (small)
+//
+// For inputs whose chunks all fit in one resident wave of warps, a warp walks
+// its chunk as the cooperative walk does and decodes it right away: the block
+// starts stay in shared memory, the staged payload serves both steps, and
+// neither the records nor a third launch are needed. While one warp decodes,
+// the other warps of its SM are still walking, so the decode hides under the
+// walks' latency.
+constexpr uint32_t kFusedWarps = 4;
+static_assert(kStageWords == kCoopStageWords, "the walk and the decode read the same staged payload");
+
+template <bool W16>
+__global__ void __launch_bounds__(kFusedWarps * 32, 6)
+    walk_decode_kernel(DecodeArgs p) {
+  __shared__ __align__(128) uint32_t tile[kFusedWarps][32 * 32];  // per warp: 32 lane rows of 128 B
+  __shared__ __align__(16) uint32_t stage[kFusedWarps][kStageWords];  // per warp: the chunk's payload
+  __shared__ uint16_t starts[kFusedWarps][32];  // start bit of block b >= 1
+  __shared__ __align__(8) unsigned long long mbar[kFusedWarps];
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t C = p.num_chunks;
+  const uint32_t c = blockIdx.x * kFusedWarps + warp;
+  if (c >= C) return;
+  const uint64_t off = 2ull * C + sizes_before_chunk(p, c, lane);
+  const uint32_t L = __ldg(reinterpret_cast<const uint16_t *>(p.in) + c);
+  const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
+  if (L == 0 || L > raw_len || off + L > p.comp_bytes) {
+    if (lane == 0) atomicMax(p.status, kErrCorrupt);
+    return;
   }
-  if (!ok) atomicMax(p.status, kErrCorrupt);
+  uint8_t *dst = p.out + (uint64_t)c * 4096u;
+  if (L == raw_len) {
+    copy_raw_chunk(p.in, off, raw_len, dst, lane);
+    return;
+  }
+  const uint64_t a0 = off & ~15ull;
+  const uint32_t bytes = (uint32_t)(((off + L + 15) & ~15ull) - a0);  // <= 4112
+  const uint32_t mb = smem_u32(&mbar[warp]);
+  const uint32_t sbase = smem_u32(stage[warp]);
+  if (lane == 0) {
+    mbar_init(mb, 1);
+    fence_mbar_init();
+  }
   __syncwarp();
-  // coalesced write-out of the chunk
-#pragma unroll
-  for (uint32_t i = 0; i < 8; ++i) {
-    const uint32_t v = lane + 32u * i;
-    if (16u * v >= raw_len) break;
-    const uint4 q = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(tw) + tile_swz(v >> 3, v & 7));
-    if (16u * v + 16u <= raw_len) {
-      *reinterpret_cast<uint4 *>(dst + 16u * v) = q;
-    } else {
-      const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
-      for (uint32_t b = 0; 16u * v + b < raw_len; ++b) dst[16u * v + b] = (uint8_t)(qq[b >> 2] >> ((b & 3) * 8));
-    }
+  if (lane == 0) {
+    mbar_arrive_expect_tx(mb, bytes);
+    bulk_load(sbase, p.in + a0, bytes, mb);
   }
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait(mb, 0, kMbarPolls))) {
+    mbar_wait(mb, 0, kMbarPolls);  // leave no copy in flight
+    if (lane == 0) atomicMax(p.status, kErrTimeout);
+    return;
+  }
+  const uint32_t bit0 = (uint32_t)(off - a0) * 8u;
+  const uint32_t nblk = (raw_len + 127u) >> 7;
+  uint16_t *ts = starts[warp];
+  const bool ok = coop_walk<W16>(stage[warp], bit0, L, nblk, lane, [ts, lane](uint32_t b, uint32_t pos) {
+    if (lane == 0) ts[b] = (uint16_t)pos;
+  });
+  if (!ok) {  // warp-uniform
+    if (lane == 0) atomicMax(p.status, kErrCorrupt);
+    return;
+  }
+  __syncwarp();
+  const uint32_t s0 = (lane >= 1 && lane < nblk) ? ts[lane] : 0u;
+  const uint32_t s1 = (lane + 1 < nblk) ? ts[lane + 1] : 0u;
+  if (!decode_staged<W16>(sbase, bit0, s0, s1, nblk, L, raw_len, tile[warp], dst, lane))
+    atomicMax(p.status, kErrCorrupt);
 }
 
 template __global__ void walk_kernel<false>(DecodeArgs);
+template __global__ void walk_decode_kernel<false>(DecodeArgs);
+template __global__ void walk_decode_kernel<true>(DecodeArgs);
 template __global__ void walk_coop_kernel<false>(DecodeArgs);
 template __global__ void walk_coop_kernel<true>(DecodeArgs);
 template __global__ void walk_kernel<true>(DecodeArgs);
@@ -1025,6 +1126,11 @@ int walk_threads() { return kWalkWarps * 32; }
 uint32_t coop_max_chunks() { return kCoopMaxChunks; }
 int coop_warps() { return kCoopWarps; }
 size_t coop_smem_bytes() { return kCoopSmem; }
+int fused_warps() { return kFusedWarps; }
+const void *walk_decode_kernel_ptr(bool w16) {
+  return w16 ? reinterpret_cast<const void *>(&walk_decode_kernel<true>)
+             : reinterpret_cast<const void *>(&walk_decode_kernel<false>);
+}
 const void *walk_coop_kernel_ptr(bool w16) {
   return w16 ? reinterpret_cast<const void *>(&walk_coop_kernel<true>)
              : reinterpret_cast<const void *>(&walk_coop_kernel<false>);

@@ -48,6 +48,8 @@ uint32_t coop_max_chunks();           // inputs up to this many chunks use the c
 int coop_warps();                     // chunks per cooperative-walk block (one warp each)
 size_t coop_smem_bytes();
 const void *walk_coop_kernel_ptr(bool w16);
+int fused_warps();                    // chunks per fused walk-and-decode block (one warp each)
+const void *walk_decode_kernel_ptr(bool w16);  // small inputs: walk and decode in one launch
 const void *size_sum_kernel_ptr();    // 256 threads, one block per group but the last
 int decode_threads();
 int decode_chunks_per_cta();

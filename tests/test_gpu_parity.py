@@ -189,9 +189,10 @@ def test_corrupt_streams_report_status():
 @pytest.mark.parametrize("dtype,ew", [("fp32", 4), ("bf16", 2)])
 def test_corrupt_attention_streams_on_the_cooperative_walk(dtype, ew):
     # 1,024 / 512 chunks of causal attention (DBX and BX blocks with runs of
-    # short codes, parsed several per step by the cooperative warp walk): one
-    # random bit flipped per call anywhere past the size table, judged by the
-    # oracle on the whole stream.
+    # short codes, parsed several per step by the cooperative warp walk; at
+    # this size one resident wave of warps walks and decodes every chunk in a
+    # single launch): one random bit flipped per call anywhere past the size
+    # table, judged by the oracle on the whole stream.
     t = W.sweep_segment("attention", dtype, seed=41, seg_bytes=(4 if dtype == "fp32" else 2) << 20)
     data = t.data.tobytes()
     n = len(data)
@@ -210,6 +211,39 @@ def test_corrupt_attention_streams_on_the_cooperative_walk(dtype, ew):
         assert st == rc_ref, pos
         if st == 0:
             assert out == out_ref
+
+
+@pytest.mark.parametrize("dtype,seg_mib", [("fp32", 22), ("bf16", 20)])
+def test_corrupt_attention_streams_on_the_standalone_cooperative_walk(dtype, seg_mib):
+    # 5,632 / 5,120 chunks: more than one resident wave of the fused walk and
+    # decode (6 blocks of 4 warps per SM on 152 SMs), so the cooperative walk
+    # runs as a launch of its own and the decode kernel follows it. Clean
+    # round trip first, then one bit flipped per call in the last chunks,
+    # each flip judged by the oracle on the flipped chunk alone.
+    t = W.sweep_segment("attention", dtype, seed=47, seg_bytes=seg_mib << 20)
+    ew = t.elem_width
+    data = t.data
+    n = data.size
+    s = bytearray(oracle.compress(data, ew))
+    lens, offs = chunk_table(bytes(s), n)
+    C = lens.size
+    assert 3648 < C <= 6144
+    st, back = gpu_decompress(bytes(s), n, ew)
+    assert st == 0 and back == data.tobytes()
+    rng = np.random.default_rng(53)
+    for _ in range(32):
+        c = int(rng.integers(C - 256, C))
+        L = int(lens[c])
+        bad = bytearray(s)
+        bit = int(rng.integers(0, 8 * L))
+        bad[offs[c] + bit // 8] ^= 1 << (bit % 8)
+        st, out = gpu_decompress(bytes(bad), n, ew)
+        piece = data[4096 * c: 4096 * c + 4096]
+        mini = int(L).to_bytes(2, "little") + bytes(bad[offs[c]: offs[c] + L])
+        rc_ref, out_ref = oracle.decompress_status(mini, piece.size, ew)
+        assert st == rc_ref, (c, bit)
+        if st == 0:
+            assert out[4096 * c: 4096 * c + piece.size] == out_ref
 
 
 def test_corrupt_streams_report_status_above_the_cooperative_walk_size():
