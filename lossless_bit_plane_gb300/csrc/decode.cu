@@ -19,7 +19,8 @@
 //    warp-wide by bulk copies; a step takes a block header and up to two
 //    non-verbatim codes and skips a run of verbatim codes by testing their
 //    flag bits. Up to 6144 chunks: WARP = CHUNK, the 32 lanes testing 32
-//    flags at once (shorter chains for small inputs).
+//    flags at once (shorter chains for small inputs). Where every chunk has
+//    a resident warp, that warp also decodes its chunk in the same launch.
 //  - Records: a chunk's payload offset and its blocks' start bits go into
 //    the first 72 bytes of the chunk's own output region; the decode warp
 //    reads them before it overwrites those bytes.
