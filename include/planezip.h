@@ -245,7 +245,8 @@ pz_status pz_test_lookback_timeout(const void *d_in, size_t nbytes,
  *   nbytes        must be <= PZ_NOALLOC_MAX_BYTES, else PZ_ERR_CAPACITY
  *                 (nothing is enqueued).
  * The call allocates nothing (no cudaMalloc, no allocating library call);
- * it clears the scratch it needs with cudaMemsetAsync on `stream`.
+ * it clears the scratch it needs with a kernel of its own on `stream`,
+ * launched just before the encoder.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture. All calls in the process share the one array

@@ -86,9 +86,24 @@ cudaError_t device_info(DeviceInfo &out) {
 // The 2D tensor map over the input (rows of 128 bytes; 32 x u32 each) and
 // the encoder launch. `units` is the number of chunks the launch visits
 // (every chunk, or every stride-th for sizes only); a.in, a.nbytes and
-// a.num_chunks are set by the caller.
-pz_status launch_encoder(pz::EncodeArgs &a, bool w16, bool size_only, size_t units, const DeviceInfo &info,
-                         cudaStream_t s) {
+// a.num_chunks are set by the caller. The encoder's look-back words and
+// ticket (scratch_words 8-byte words at a.status) and *a.total are zeroed by
+// a small kernel launched first; the encoder is launched as its programmatic
+// dependent, so that its launch overlaps the zeroing (its warps wait for the
+// zeroing to end before their first ticket or store).
+pz_status launch_encoder(pz::EncodeArgs &a, bool w16, bool size_only, size_t units, size_t scratch_words,
+                         const DeviceInfo &info, cudaStream_t s) {
+  {
+    unsigned long long *zp = a.status;
+    uint32_t zn = (uint32_t)scratch_words;
+    unsigned long long *zt = a.total;
+    void *zargs[3] = {&zp, &zn, &zt};
+    size_t zb = (scratch_words + 255) / 256;
+    if (zb < 1) zb = 1;
+    if (zb > (size_t)info.sms * 4) zb = (size_t)info.sms * 4;
+    if (cudaLaunchKernel(pz::zero_scratch_kernel_ptr(), dim3((unsigned)zb), dim3(256), zargs, 0, s) != cudaSuccess)
+      return PZ_ERR_CUDA;
+  }
   a.tma_rows = a.nbytes / 128;
   alignas(64) CUtensorMap tmap;
   std::memset(&tmap, 0, sizeof(tmap));
@@ -107,9 +122,17 @@ pz_status launch_encoder(pz::EncodeArgs &a, bool w16, bool size_only, size_t uni
   const size_t need = (units + warps - 1) / warps;
   if (grid > need) grid = need;
   void *args[2] = {&tmap, &a};
-  if (cudaLaunchKernel(pz::encode_kernel_ptr(w16, size_only), dim3((unsigned)grid), dim3(pz::encode_threads()), args,
-                       pz::encode_smem_bytes(w16), s) != cudaSuccess)
-    return PZ_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(pz::encode_threads());
+  cfg.dynamicSmemBytes = pz::encode_smem_bytes(w16);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, pz::encode_kernel_ptr(w16, size_only), args) != cudaSuccess) return PZ_ERR_CUDA;
   return PZ_OK;
 }
 
@@ -137,15 +160,14 @@ pz_status pz_compress_candidates(const void *d_in, size_t nbytes, int elem_width
   if (C > 0x7FFFFFFFu || nbytes / 128 > 0xFFFFFFFFull) return PZ_ERR_ARG;
   if (out_capacity < pz_max_compressed_bytes(nbytes)) return PZ_ERR_CAPACITY;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
-  if (nbytes == 0) return PZ_OK;
+  if (nbytes == 0)
+    return cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) == cudaSuccess ? PZ_OK : PZ_ERR_CUDA;
 
   DeviceInfo info;
   if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
 
   uint8_t *out = static_cast<uint8_t *>(d_out);
   uint8_t *scratch = out + align16(2 * C + nbytes);
-  if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
 
   pz::EncodeArgs a{};
   a.in = static_cast<const uint8_t *>(d_in);
@@ -157,7 +179,7 @@ pz_status pz_compress_candidates(const void *d_in, size_t nbytes, int elem_width
   a.num_chunks = (uint32_t)C;
   a.candidates = candidates | PZ_CAND_RAW;
   a.stride = 1;
-  return launch_encoder(a, elem_width == 2, false, C, info, s);
+  return launch_encoder(a, elem_width == 2, false, C, C + 8, info, s);
 }
 
 pz_status pz_test_lookback_timeout(const void *d_in, size_t nbytes, int elem_width, void *d_out, size_t out_capacity,
@@ -168,18 +190,14 @@ pz_status pz_test_lookback_timeout(const void *d_in, size_t nbytes, int elem_wid
   if (!aligned16(d_in) || !aligned16(d_out)) return PZ_ERR_ARG;
   if (out_capacity < pz_max_compressed_bytes(nbytes)) return PZ_ERR_CAPACITY;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
   DeviceInfo info;
   if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
   uint8_t *out = static_cast<uint8_t *>(d_out);
   uint8_t *scratch = out + align16(2 * C + nbytes);
-  if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
-  // the ticket starts at 1: chunk 0 is never taken, so its status word is
-  // never published
-  static const unsigned int kOne = 1;
-  if (cudaMemcpyAsync(scratch + 8 * C, &kOne, sizeof(kOne), cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return PZ_ERR_CUDA;
   pz::EncodeArgs a{};
+  // chunks are numbered from 1: chunk 0 is never taken, so its status word
+  // is never published
+  a.unit0 = 1;
   a.in = static_cast<const uint8_t *>(d_in);
   a.out = out;
   a.status = reinterpret_cast<unsigned long long *>(scratch);
@@ -189,7 +207,7 @@ pz_status pz_test_lookback_timeout(const void *d_in, size_t nbytes, int elem_wid
   a.num_chunks = (uint32_t)C;
   a.candidates = PZ_CAND_ALL;
   a.stride = 1;
-  return launch_encoder(a, elem_width == 2, false, C, info, s);
+  return launch_encoder(a, elem_width == 2, false, C, C + 8, info, s);
 }
 
 pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width, unsigned int candidates,
@@ -201,8 +219,7 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width, un
   if (nbytes && !aligned16(d_in)) return PZ_ERR_ARG;
   if (C > 0x7FFFFFFFu || nbytes / 128 > 0xFFFFFFFFull) return PZ_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d_total, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
-  if (nbytes == 0) return PZ_OK;
+  if (nbytes == 0) return cudaMemsetAsync(d_total, 0, sizeof(unsigned long long), s) == cudaSuccess ? PZ_OK : PZ_ERR_CUDA;
   DeviceInfo info;
   if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
   pz::EncodeArgs a{};
@@ -213,7 +230,7 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width, un
   a.candidates = candidates | PZ_CAND_RAW;
   a.stride = chunk_stride;
   a.sizes = d_sizes;
-  return launch_encoder(a, elem_width == 2, true, (C + chunk_stride - 1) / chunk_stride, info, s);
+  return launch_encoder(a, elem_width == 2, true, (C + chunk_stride - 1) / chunk_stride, 0, info, s);
 }
 
 pz_status pz_decompress(const void *d_in, size_t comp_bytes, int elem_width, void *d_out, size_t nbytes,
@@ -326,15 +343,15 @@ extern "C" pz_status pz_compress_noalloc(const void *d_in, size_t nbytes, int el
   if (nbytes > PZ_NOALLOC_MAX_BYTES) return PZ_ERR_CAPACITY;
   if (out_capacity < 2 * C + nbytes) return PZ_ERR_CAPACITY;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) != cudaSuccess) return PZ_ERR_CUDA;
-  if (nbytes == 0) return PZ_OK;
+  if (nbytes == 0)
+    return cudaMemsetAsync(d_total_bytes, 0, sizeof(unsigned long long), s) == cudaSuccess ? PZ_OK : PZ_ERR_CUDA;
 
   DeviceInfo info;
   if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
   void *scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess) return PZ_ERR_CUDA;
-  // the previous call's look-back words and ticket must not leak into this one
-  if (cudaMemsetAsync(scratch, 0, 8 * C + 64, s) != cudaSuccess) return PZ_ERR_CUDA;
+  // the previous call's look-back words and ticket must not leak into this
+  // one: the encoder launch zeroes them first
 
   pz::EncodeArgs a{};
   a.in = static_cast<const uint8_t *>(d_in);
@@ -346,5 +363,5 @@ extern "C" pz_status pz_compress_noalloc(const void *d_in, size_t nbytes, int el
   a.num_chunks = (uint32_t)C;
   a.candidates = PZ_CAND_ALL;
   a.stride = 1;
-  return launch_encoder(a, elem_width == 2, false, C, info, s);
+  return launch_encoder(a, elem_width == 2, false, C, C + 8, info, s);
 }

@@ -9,9 +9,12 @@
 //
 // GPU design (one kernel does load, classify, select, emit, scan, scatter):
 //  - Persistent warps take chunks in ticket order (atomic counter), the next
-//    ticket only once the current chunk is done. A warp owns a 4 KB chunk;
-//    LANE b OWNS BLOCK b and works on it alone, so the per-block work is SIMD
-//    over 32 blocks rather than cooperative.
+//    ticket only once the current chunk is done. The launch is the
+//    programmatic dependent of the small kernel that zeroes the look-back
+//    words, the ticket and the total, so that its launch overlaps that
+//    kernel; each warp waits for it before its first ticket. A warp owns a
+//    4 KB chunk; LANE b OWNS BLOCK b and works on it alone, so the per-block
+//    work is SIMD over 32 blocks rather than cooperative.
 //  - The chunk arrives by a 2D TMA tile load (32 rows x 128 B, 128-byte
 //    swizzle) into the warp's shared stage; the other warps of the SM cover
 //    its latency, and each warp prefetches into L2 the chunk one wave of
@@ -788,6 +791,19 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t u) {
   return r * 128u + ((u ^ (r & 7u)) << 4);
 }
 
+// Programmatic dependent launch: the encoder is launched as the dependent of
+// the kernel that zeroes its scratch words, and may start before that kernel
+// ends; griddepcontrol.wait returns once it has ended and its stores are
+// visible (at once when the launch had no such predecessor).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__global__ void zero_scratch_kernel(unsigned long long *scratch, uint32_t nwords, unsigned long long *total) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
+  for (uint32_t i = i0; i < nwords; i += gridDim.x * blockDim.x) scratch[i] = 0;
+  if (i0 == 0) *total = 0;
+}
+
 // kSizeOnly: the sizes-only launch (no stream). It classifies chunks 0,
 // stride, 2*stride, ... (warps take them in a fixed round-robin, no ticket),
 // and reports each L and the sum of 2 + L, without emitting, locating or
@@ -850,11 +866,18 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     if (kSizeOnly) return u + nwarps;
     uint32_t v = 0;
     if (lane == 0) v = atomicAdd(p.ticket, 1u);
-    return __shfl_sync(0xFFFFFFFFu, v, 0);
+    return p.unit0 + __shfl_sync(0xFFFFFFFFu, v, 0);
   };
   auto chunk_of = [&](uint32_t u) -> uint32_t { return kSizeOnly ? u * p.stride : u; };
   unsigned long long size_sum = 0;  // sizes only: this warp's sum of 2 + L
 
+  // the ticket counter is zeroed by the preceding kernel: wait for it before
+  // the first ticket (the sizes-only launch waits before its first store)
+  bool scratch_ready = false;
+  if (!kSizeOnly) {
+    griddep_wait();
+    scratch_ready = true;
+  }
   uint32_t u = kSizeOnly ? warp_id : next_unit(0);
   if (u < U) issue(chunk_of(u));
 
@@ -889,6 +912,10 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     uint32_t L = (total_bits + 7) >> 3;
     const bool raw_chunk = L >= raw_len;
     if (raw_chunk) L = raw_len;
+    if (!scratch_ready) {  // sizes only: before the first store to the sizes or the total
+      griddep_wait();
+      scratch_ready = true;
+    }
     if (kSizeOnly) {
       if (lane == 0) {
         if (p.sizes) p.sizes[u] = (uint16_t)L;
@@ -962,6 +989,7 @@ size_t encode_smem_bytes(bool w16) { return w16 ? EncCfg<true>::kBytes : EncCfg<
 int encode_threads() { return kEncWarps * 32; }
 int encode_warps() { return kEncWarps; }
 
+const void *zero_scratch_kernel_ptr() { return reinterpret_cast<const void *>(&zero_scratch_kernel); }
 const void *encode_kernel_ptr(bool w16, bool size_only) {
   if (size_only)
     return w16 ? reinterpret_cast<const void *>(&encode_kernel<true, true>)

@@ -16,6 +16,9 @@ struct EncodeArgs {
   unsigned long long *status;    // look-back words, one per chunk, zeroed
   unsigned int *ticket;          // chunk ticket counter, zeroed
   unsigned long long *total;     // stream length (atomicMax target), zeroed
+  // ticket k stands for chunk unit0 + k (nonzero only to leave the first
+  // chunks unprocessed)
+  uint32_t unit0;
   uint64_t nbytes;
   uint64_t tma_rows;             // 128-byte rows covered by the tensor map (0: none)
   uint32_t num_chunks;
@@ -39,6 +42,9 @@ size_t encode_smem_bytes(bool w16);
 int encode_threads();
 int encode_warps();
 const void *encode_kernel_ptr(bool w16, bool size_only);
+// zero_scratch_kernel(scratch, nwords, total): zeroes nwords 8-byte words
+// and *total, and lets its programmatic dependent (the encoder) start at once
+const void *zero_scratch_kernel_ptr();
 
 int walk_threads();
 size_t walk_smem_bytes();
