@@ -722,8 +722,12 @@ __device__ __forceinline__ uint64_t lookback(unsigned long long *status, uint32_
       __nanosleep(64);
       continue;
     }
-    uint64_t val = (lane <= firstP) ? (v & kValueMask) : 0ull;
-    excl += warp_sum_u64(val);
+    // the words before the first inclusive one are chunk sizes (at most 4096
+    // each), so their sum fits one 32-bit warp reduction; the inclusive
+    // word's value comes from its lane
+    const uint32_t sizes = (lane < firstP) ? (uint32_t)(v & kValueMask) : 0u;
+    const uint64_t inc = (firstP < 32) ? (__shfl_sync(0xFFFFFFFFu, v, firstP) & kValueMask) : 0ull;
+    excl += (uint64_t)__reduce_add_sync(0xFFFFFFFFu, sizes) + inc;
     if (firstP < 32) break;
     base -= 32;
   }
