@@ -83,6 +83,24 @@ cudaError_t device_info(DeviceInfo &out) {
   return cudaSuccess;
 }
 
+// One kernel launch; with `dependent` it is the programmatic dependent of
+// the kernel launched just before it on the stream (the kernel waits for
+// that one with griddepcontrol.wait before it touches its results).
+cudaError_t launch(const void *fn, size_t grid, size_t threads, size_t smem, void **args, bool dependent,
+                   cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // The 2D tensor map over the input (rows of 128 bytes; 32 x u32 each) and
 // the encoder launch. `units` is the number of chunks the launch visits
 // (every chunk, or every stride-th for sizes only); a.in, a.nbytes and
@@ -122,17 +140,9 @@ pz_status launch_encoder(pz::EncodeArgs &a, bool w16, bool size_only, size_t uni
   const size_t need = (units + warps - 1) / warps;
   if (grid > need) grid = need;
   void *args[2] = {&tmap, &a};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(pz::encode_threads());
-  cfg.dynamicSmemBytes = pz::encode_smem_bytes(w16);
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelExC(&cfg, pz::encode_kernel_ptr(w16, size_only), args) != cudaSuccess) return PZ_ERR_CUDA;
+  if (launch(pz::encode_kernel_ptr(w16, size_only), grid, (size_t)pz::encode_threads(), pz::encode_smem_bytes(w16),
+             args, true, s) != cudaSuccess)
+    return PZ_ERR_CUDA;
   return PZ_OK;
 }
 
@@ -268,30 +278,36 @@ pz_status pz::decompress_launch(const void *d_in, size_t comp_bytes, int elem_wi
   void *args[1] = {&a};
   const size_t G = pz::group_chunks();
   const size_t groups = (C + G - 1) / G;
+  // Each launch after the first kernel is its predecessor's programmatic
+  // dependent: its blocks are scheduled while the predecessor runs and wait
+  // for its end (griddepcontrol.wait) before they start, which hides the
+  // launch gap. The first kernel follows the status memset and is launched
+  // plainly.
   if (groups > 1 && cudaLaunchKernel(pz::size_sum_kernel_ptr(), dim3((unsigned)(groups - 1)), dim3(256), args, 0,
                                      s) != cudaSuccess)
     return PZ_ERR_CUDA;
+  const bool after_kernel = groups > 1;
   if (C <= info.fused_max_chunks[w16 ? 1 : 0]) {  // one resident wave: a warp walks and decodes each chunk
     const size_t fw = (size_t)pz::fused_warps();
-    if (cudaLaunchKernel(pz::walk_decode_kernel_ptr(w16), dim3((unsigned)((C + fw - 1) / fw)),
-                         dim3((unsigned)(32 * fw)), args, 0, s) != cudaSuccess)
+    if (launch(pz::walk_decode_kernel_ptr(w16), (C + fw - 1) / fw, 32 * fw, 0, args, after_kernel, s) !=
+        cudaSuccess)
       return PZ_ERR_CUDA;
     return PZ_OK;
   }
   if (C <= pz::coop_max_chunks()) {  // small input: a warp walks each chunk
     const size_t cw = (size_t)pz::coop_warps();
-    if (cudaLaunchKernel(pz::walk_coop_kernel_ptr(w16), dim3((unsigned)((C + cw - 1) / cw)), dim3((unsigned)(32 * cw)),
-                         args, pz::coop_smem_bytes(), s) != cudaSuccess)
+    if (launch(pz::walk_coop_kernel_ptr(w16), (C + cw - 1) / cw, 32 * cw, pz::coop_smem_bytes(), args, after_kernel,
+               s) != cudaSuccess)
       return PZ_ERR_CUDA;
   } else {  // a thread walks each chunk
     const size_t wt = (size_t)pz::walk_threads();
-    if (cudaLaunchKernel(pz::walk_kernel_ptr(w16), dim3((unsigned)((C + wt - 1) / wt)), dim3((unsigned)wt), args,
-                         pz::walk_smem_bytes(), s) != cudaSuccess)
+    if (launch(pz::walk_kernel_ptr(w16), (C + wt - 1) / wt, wt, pz::walk_smem_bytes(), args, after_kernel, s) !=
+        cudaSuccess)
       return PZ_ERR_CUDA;
   }
   const size_t per = (size_t)pz::decode_chunks_per_cta();
-  if (cudaLaunchKernel(pz::decode_kernel_ptr(w16), dim3((unsigned)((C + per - 1) / per)),
-                       dim3(pz::decode_threads()), args, 0, s) != cudaSuccess)
+  if (launch(pz::decode_kernel_ptr(w16), (C + per - 1) / per, (size_t)pz::decode_threads(), 0, args, true, s) !=
+      cudaSuccess)
     return PZ_ERR_CUDA;
   return PZ_OK;
 }

@@ -450,6 +450,7 @@ __device__ __forceinline__ unsigned long long sum8_sizes(const uint4 v) {
 
 __global__ void __launch_bounds__(256) size_sum_kernel(DecodeArgs p) {
   __shared__ unsigned long long red[8];
+  griddep_launch_dependents();  // the walk's blocks may be scheduled now; they wait for this kernel's end
   const uint32_t g = blockIdx.x;  // every chunk of the group exists
   const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.in) + (uint64_t)g * (kGroupChunks / 8) + threadIdx.x);
   const unsigned long long s = warp_sum_u64(sum8_sizes(v));
@@ -660,6 +661,8 @@ template <bool W16>
 __global__ void __launch_bounds__(kWalkWarps * 32)
     walk_kernel(DecodeArgs p) {
   extern __shared__ __align__(128) uint8_t walk_smem[];
+  griddep_launch_dependents();  // the decode's blocks may be scheduled now
+  griddep_wait();               // the group sums are complete
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t *win = reinterpret_cast<const uint32_t *>(walk_smem) + (warp * 32u + lane) * kWinStride;
   const uint32_t mb = smem_u32(walk_smem + kWalkWarps * 32 * kWinStride * 4) + warp * 8u;
@@ -822,6 +825,8 @@ template <bool W16>
 __global__ void __launch_bounds__(kCoopWarps * 32)
     walk_coop_kernel(DecodeArgs p) {
   extern __shared__ __align__(128) uint8_t coop_smem[];
+  griddep_launch_dependents();  // the decode's blocks may be scheduled now
+  griddep_wait();               // the group sums are complete
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t C = p.num_chunks;
   const uint32_t c = blockIdx.x * kCoopWarps + warp;
@@ -971,6 +976,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
   __shared__ __align__(128) uint32_t tile[kDecWarps][32 * 32];  // per warp: 32 lane rows of 128 B
   __shared__ __align__(16) uint32_t stage[kDecWarps][kStageWords];  // per warp: the chunk's payload
   __shared__ uint16_t tail_starts[kDecWarps][32];
+  griddep_wait();  // the walk's records are complete
   const uint32_t lane = lane_id();
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t C = p.num_chunks;
@@ -1063,6 +1069,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 6)
   __shared__ __align__(16) uint32_t stage[kFusedWarps][kStageWords];  // per warp: the chunk's payload
   __shared__ uint16_t starts[kFusedWarps][32];  // start bit of block b >= 1
   __shared__ __align__(8) unsigned long long mbar[kFusedWarps];
+  griddep_wait();  // the group sums are complete
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t C = p.num_chunks;
   const uint32_t c = blockIdx.x * kFusedWarps + warp;

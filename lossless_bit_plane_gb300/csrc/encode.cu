@@ -795,14 +795,10 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t u) {
   return r * 128u + ((u ^ (r & 7u)) << 4);
 }
 
-// Programmatic dependent launch: the encoder is launched as the dependent of
-// the kernel that zeroes its scratch words, and may start before that kernel
-// ends; griddepcontrol.wait returns once it has ended and its stores are
-// visible (at once when the launch had no such predecessor).
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
+// The encoder is launched as the programmatic dependent of the kernel that
+// zeroes its scratch words, and may start before that kernel ends.
 __global__ void zero_scratch_kernel(unsigned long long *scratch, uint32_t nwords, unsigned long long *total) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  griddep_launch_dependents();
   const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
   for (uint32_t i = i0; i < nwords; i += gridDim.x * blockDim.x) scratch[i] = 0;
   if (i0 == 0) *total = 0;

@@ -150,6 +150,18 @@ struct BitWriter {
   }
 };
 
+// --------------------------------------------- programmatic dependent launch
+// A kernel launched with the programmatic-serialization attribute right after
+// another kernel of the same stream may start before that kernel ends:
+// griddepcontrol.wait returns once the predecessor has ended and its stores
+// are visible (at once when the launch had no such predecessor), and a
+// predecessor's griddepcontrol.launch_dependents lets the dependent's blocks
+// be scheduled before it ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------ global memory, relaxed
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
   unsigned long long v;
