@@ -45,7 +45,7 @@ WORKLOAD = ("1 GiB throughput sweep: {ReLU, smooth conv, causal attention} x {FP
 # ncu capture per segment workload (profiles/dram_bytes_per_kernel_sweep_segments.md).
 # It describes the current encode kernel only; it is reported when the sweep's
 # dominant call is the encoder and null otherwise.
-NCU_TRAFFIC_BYTES_PER_LAUNCH = 208.52e6
+NCU_TRAFFIC_BYTES_PER_LAUNCH = 208.32e6
 
 
 def parse():
