@@ -215,9 +215,11 @@ def test_corrupt_attention_streams_on_the_cooperative_walk(dtype, ew):
 
 @pytest.mark.parametrize("dtype,seg_mib", [("fp32", 22), ("bf16", 20)])
 def test_corrupt_attention_streams_on_the_standalone_cooperative_walk(dtype, seg_mib):
-    # 5,632 / 5,120 chunks: more than one resident wave of the fused walk and
-    # decode (6 blocks of 4 warps per SM on 152 SMs), so the cooperative walk
-    # runs as a launch of its own and the decode kernel follows it. Clean
+    # 5,120 chunks (whole 1024 x 1024 attention matrices: 20 MiB of FP32 from
+    # the 22 MiB asked for, 20 MiB of BF16): more than one resident wave of
+    # the fused walk and decode (6 blocks of 4 warps per SM on 152 SMs), so
+    # the cooperative walk runs as a launch of its own and the decode kernel
+    # follows it. Clean
     # round trip first, then one bit flipped per call in the last chunks,
     # each flip judged by the oracle on the flipped chunk alone.
     t = W.sweep_segment("attention", dtype, seed=47, seg_bytes=seg_mib << 20)
@@ -305,6 +307,41 @@ def test_corrupt_attention_streams_above_the_cooperative_walk_size(dtype, seg_mi
         assert st == rc_ref, (c, bit)
         if st == 0:
             assert out[4096 * c: 4096 * c + piece.size] == out_ref
+
+
+def test_calls_queued_back_to_back_on_one_stream():
+    # Compress and decompress calls of four sizes, one per decode path (the
+    # fused walk and decode alone and after the size sums, the standalone
+    # cooperative walk, the thread walk), queued on one stream with no host
+    # synchronisation: each call's first kernel follows the previous call's
+    # last one, and the kernels inside a call are launched as programmatic
+    # dependents. Every stream equals the oracle's (sampled chunks for the two
+    # larger inputs) and every round trip is exact.
+    rng = np.random.default_rng(61)
+    items = [(W.relu_values(256 * 1024, rng).view(np.uint8), 4),
+             (W.conv_bf16().data.view(np.uint8), 2),
+             (W.sweep_segment("attention", "fp32", seed=67, seg_bytes=20 << 20).data.view(np.uint8), 4),
+             (W.sweep_segment("attention", "bf16", seed=71, seg_bytes=34 << 20).data.view(np.uint8), 2)]
+    assert [(a.size + 4095) // 4096 for a, _ in items] == [256, 3136, 5120, 8704]
+    xs = [to_device(a) for a, _ in items]
+    torch.cuda.synchronize()
+    results = []
+    for _ in range(2):
+        for x, (a, ew) in zip(xs, items):
+            out, total = _lib.compress_tensor(x, ew)
+            back, st = _lib.decompress_tensor(out, out.numel(), ew, a.size)
+            results.append((x, out, total, back, st, a, ew))
+    torch.cuda.synchronize()
+    for x, out, total, back, st, a, ew in results:
+        n = int(total.item())
+        assert int(st.item()) == 0
+        assert torch.equal(back[: a.size], x)
+        stream = out[:n].cpu().numpy().tobytes()
+        C = (a.size + 4095) // 4096
+        if C <= 3136:
+            assert stream == oracle.compress(a.tobytes(), ew)
+        else:
+            sampled_chunk_parity(a, ew, stream, list(range(0, C, 97)) + [C - 1])
 
 
 def test_repeated_calls_and_streams_are_deterministic():
