@@ -111,17 +111,6 @@ cudaError_t launch(const void *fn, size_t grid, size_t threads, size_t smem, voi
 // zeroing to end before their first ticket or store).
 pz_status launch_encoder(pz::EncodeArgs &a, bool w16, bool size_only, size_t units, size_t scratch_words,
                          const DeviceInfo &info, cudaStream_t s) {
-  {
-    unsigned long long *zp = a.status;
-    uint32_t zn = (uint32_t)scratch_words;
-    unsigned long long *zt = a.total;
-    void *zargs[3] = {&zp, &zn, &zt};
-    size_t zb = (scratch_words + 255) / 256;
-    if (zb < 1) zb = 1;
-    if (zb > (size_t)info.sms * 4) zb = (size_t)info.sms * 4;
-    if (cudaLaunchKernel(pz::zero_scratch_kernel_ptr(), dim3((unsigned)zb), dim3(256), zargs, 0, s) != cudaSuccess)
-      return PZ_ERR_CUDA;
-  }
   a.tma_rows = a.nbytes / 128;
   alignas(64) CUtensorMap tmap;
   std::memset(&tmap, 0, sizeof(tmap));
@@ -134,6 +123,18 @@ pz_status launch_encoder(pz::EncodeArgs &a, bool w16, bool size_only, size_t uni
                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return PZ_ERR_CUDA;
+  }
+  // a failure above leaves the stream untouched: the launches start here
+  {
+    unsigned long long *zp = a.status;
+    uint32_t zn = (uint32_t)scratch_words;
+    unsigned long long *zt = a.total;
+    void *zargs[3] = {&zp, &zn, &zt};
+    size_t zb = (scratch_words + 255) / 256;
+    if (zb < 1) zb = 1;
+    if (zb > (size_t)info.sms * 4) zb = (size_t)info.sms * 4;
+    if (cudaLaunchKernel(pz::zero_scratch_kernel_ptr(), dim3((unsigned)zb), dim3(256), zargs, 0, s) != cudaSuccess)
+      return PZ_ERR_CUDA;
   }
   const int warps = pz::encode_warps();
   size_t grid = (size_t)info.enc_ctas_per_sm[2 * (size_only ? 1 : 0) + (w16 ? 1 : 0)] * info.sms;
