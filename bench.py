@@ -42,10 +42,28 @@ WORKLOAD = ("1 GiB throughput sweep: {ReLU, smooth conv, causal attention} x {FP
 
 # DRAM bytes (read + write) per encoder launch on the 1 GiB sweep: the mean
 # over its seven segments of dram__bytes_read.sum + dram__bytes_write.sum, one
-# ncu capture per segment workload (profiles/dram_bytes_per_kernel_sweep_segments.md).
-# It describes the current encode kernel only; it is reported when the sweep's
-# dominant call is the encoder and null otherwise.
-NCU_TRAFFIC_BYTES_PER_LAUNCH = 208.32e6
+# ncu capture of the encoder per segment workload. The counters describe the
+# encoder as compiled from the device sources whose sha256 is recorded with
+# them: once those sources change, `roofline.traffic` is reported as null
+# until the encoder is captured again. It is also null when the sweep's
+# dominant call is not the encoder.
+NCU_ENCODER_TRAFFIC = {
+    "sources": ("lossless_bit_plane_gb300/csrc/encode.cu", "lossless_bit_plane_gb300/csrc/pz_device.cuh",
+                "lossless_bit_plane_gb300/csrc/pz_format.cuh"),
+    "sources_sha256": "0ae8796a719666857273a4e5ef7b7131b1f7fb92ac0dfb35576670d19c9c25b1",
+    "bytes_per_launch": 208.32e6,
+}
+
+
+def encoder_traffic():
+    """The recorded ncu DRAM bytes per encoder launch, or None if the
+    encoder's device sources are not the ones they were measured on."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in NCU_ENCODER_TRAFFIC["sources"]:
+        h.update((ROOT / f).read_bytes())
+    return NCU_ENCODER_TRAFFIC["bytes_per_launch"] if h.hexdigest() == NCU_ENCODER_TRAFFIC["sources_sha256"] else None
 
 
 def parse():
@@ -61,6 +79,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the sizes-only, ablation and swap sections (run after the timed region)")
+    ap.add_argument("--seg-mib", type=int, default=128,
+                    help="segment size in MiB for a single-segment workload (<kind>_<dtype>; attention wants a "
+                         "multiple of 4 MiB for FP32 and 2 MiB for BF16); small profiling cases")
     ap.add_argument("--workload", default="sweep",
                     help="'sweep' (the 1 GiB sweep, the headline), a parity config (config1, config2, config3, "
                          "config4_fp32, config4_bf16), or one sweep segment as <kind>_<dtype>, e.g. "
@@ -163,7 +184,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload
 
-def make_workload(name: str = "sweep"):
+def make_workload(name: str = "sweep", seg_mib: int = 128):
     from lossless_bit_plane_gb300 import workloads as W
 
     if name == "sweep":
@@ -174,7 +195,7 @@ def make_workload(name: str = "sweep"):
     if name in configs:
         return configs[name]()
     kind, dtype = name.rsplit("_", 1)
-    return [W.sweep_segment(kind, dtype)]
+    return [W.sweep_segment(kind, dtype, seg_bytes=seg_mib << 20)]
 
 
 CONFIG_LABELS = {
@@ -189,7 +210,7 @@ CONFIG_LABELS = {
 def workload_label(name: str) -> str:
     if name == "sweep":
         return WORKLOAD
-    return CONFIG_LABELS.get(name, f"one 1 GiB-sweep segment: {name}")
+    return CONFIG_LABELS.get(name, f"one 1 GiB-sweep segment distribution: {name}")
 
 
 def peak_hbm():
@@ -265,7 +286,7 @@ def run_reference(args, rank: int):
     bounded sample of the workload per step (rank 0 only)."""
     if rank != 0:
         return 0
-    segs = make_workload(args.workload)
+    segs = make_workload(args.workload, args.seg_mib)
     mib = min(args.cpu_parallel_mib, 4.0) if args.cpu_parallel_mib > 0 else 1.0
     for _ in range(args.warmup):
         cpu_oracle_parallel(segs, mib)
@@ -304,7 +325,7 @@ def run_ours(args, rank: int, world: int, local: int):
     build.build()
     _lib.load()
 
-    segs = make_workload(args.workload)
+    segs = make_workload(args.workload, args.seg_mib)
     stream = torch.cuda.current_stream(dev)
     d_in = [torch.from_numpy(t.data).to(dev) for t in segs]
     d_out = [torch.empty(_lib.pz_max_compressed_bytes(t.nbytes), dtype=torch.uint8, device=dev) for t in segs]
@@ -449,7 +470,7 @@ def run_ours(args, rank: int, world: int, local: int):
         "ratio": raw / comp,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_kind": peak_kind,
-                     "traffic": (NCU_TRAFFIC_BYTES_PER_LAUNCH if dominant == "pz_encode" and args.workload == "sweep"
+                     "traffic": (encoder_traffic() if dominant == "pz_encode" and args.workload == "sweep"
                                  else None),
                      "encode_frac": comp_ach / peak, "decode_frac": dec_ach / peak},
         "cpu_baseline": cpu,

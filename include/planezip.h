@@ -85,7 +85,10 @@ pz_status pz_compress(const void *d_in, size_t nbytes, int elem_width,
  * Source: Section III-A "Stream format" (chunks located by a prefix sum
  * over the headers and decoded in parallel) and the inverse of each
  * candidate of Section III-A "Codec".
- *   d_in        device, comp_bytes readable; 16-byte aligned.
+ *   d_in        device, 16-byte aligned; readable up to comp_bytes rounded
+ *               up to a multiple of 16 (the decoder copies whole 16-byte
+ *               units into shared memory; an allocation of comp_bytes from
+ *               cudaMalloc or PyTorch always covers that).
  *   comp_bytes  bytes available at d_in: >= 2*C, and the stream's own
  *               length 2*C + sum(L) must not exceed it (trailing bytes are
  *               ignored).
@@ -209,20 +212,6 @@ pz_status pz_swap_out(const void *d_in, size_t nbytes, int elem_width,
 pz_status pz_swap_in(const void *h_in, size_t h_bytes, void *d_work,
                      size_t work_bytes, void *d_out, size_t nbytes,
                      int *d_status, pz_stream_t stream);
-
-/* Test hook for the bounded waits (not part of the codec; the paper has no
- * counterpart). Runs pz_compress's encoder on nbytes (2..4096 chunks) with
- * chunk 0 never taken, so that the look-back of chunk 1 waits on a status
- * word nothing publishes. That wait gives up after its iteration limit
- * (about a second) and the launch ends with *d_total_bytes = UINT64_MAX, the
- * encoder's timeout report; the GPU context stays usable. Arguments and
- * errors as pz_compress (C outside 2..4096 gives PZ_ERR_ARG); the contents
- * of d_out are unspecified afterwards. */
-pz_status pz_test_lookback_timeout(const void *d_in, size_t nbytes,
-                                   int elem_width, void *d_out,
-                                   size_t out_capacity,
-                                   unsigned long long *d_total_bytes,
-                                   pz_stream_t stream);
 
 /* Largest input pz_compress_noalloc accepts: 256 MiB (65,536 chunks). */
 #define PZ_NOALLOC_MAX_BYTES ((size_t)256 << 20)

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/planezip.h"
+#include "../../include/planezip_testing.h"
 #include "pz_kernels.h"
 
 namespace {
@@ -69,6 +70,7 @@ cudaError_t device_info(DeviceInfo &out) {
                                                              32 * pz::fused_warps(), 0)) != cudaSuccess)
         return e;
       d.fused_max_chunks[w] = (size_t)n * (size_t)d.sms * (size_t)pz::fused_warps();
+      if (d.fused_max_chunks[w] > pz::fused_max_chunks()) d.fused_max_chunks[w] = pz::fused_max_chunks();
     }
     if (!g_encode_tiled) {
       void *fn = nullptr;
@@ -277,6 +279,14 @@ pz_status pz::decompress_launch(const void *d_in, size_t comp_bytes, int elem_wi
   DeviceInfo info;
   if (device_info(info) != cudaSuccess) return PZ_ERR_CUDA;
   void *args[1] = {&a};
+  if (C <= info.fused_max_chunks[w16 ? 1 : 0]) {
+    // one resident wave: a warp walks and decodes each chunk, in one launch
+    // that reads its chunk offsets from the header table alone
+    const size_t fw = (size_t)pz::fused_warps();
+    if (launch(pz::walk_decode_kernel_ptr(w16), (C + fw - 1) / fw, 32 * fw, 0, args, false, s) != cudaSuccess)
+      return PZ_ERR_CUDA;
+    return PZ_OK;
+  }
   const size_t G = pz::group_chunks();
   const size_t groups = (C + G - 1) / G;
   // Each launch after the first kernel is its predecessor's programmatic
@@ -288,13 +298,6 @@ pz_status pz::decompress_launch(const void *d_in, size_t comp_bytes, int elem_wi
                                      s) != cudaSuccess)
     return PZ_ERR_CUDA;
   const bool after_kernel = groups > 1;
-  if (C <= info.fused_max_chunks[w16 ? 1 : 0]) {  // one resident wave: a warp walks and decodes each chunk
-    const size_t fw = (size_t)pz::fused_warps();
-    if (launch(pz::walk_decode_kernel_ptr(w16), (C + fw - 1) / fw, 32 * fw, 0, args, after_kernel, s) !=
-        cudaSuccess)
-      return PZ_ERR_CUDA;
-    return PZ_OK;
-  }
   if (C <= pz::coop_max_chunks()) {  // small input: a warp walks each chunk
     const size_t cw = (size_t)pz::coop_warps();
     if (launch(pz::walk_coop_kernel_ptr(w16), (C + cw - 1) / cw, 32 * cw, pz::coop_smem_bytes(), args, after_kernel,

@@ -1062,8 +1062,26 @@ __global__ void __launch_bounds__(kDecWarps * 32, 3)
 // neither the records nor a third launch are needed. While one warp decodes,
 // the other warps of its SM are still walking, so the decode hides under the
 // walks' latency.
+//
+// Chunk offsets come from the header table alone. Every warp of this launch
+// overwrites its chunk's output region with decoded bytes, and nothing
+// orders a warp that has finished against a warp of the same launch that has
+// not started (another stream may hold SMs, so the wave need not be resident
+// at once): no value may be read back from the output region here.
 constexpr uint32_t kFusedWarps = 4;
+constexpr uint32_t kFusedMaxChunks = 65536;  // header sums below fit 32 bits (65536 x 4096 < 2^32)
 static_assert(kStageWords == kCoopStageWords, "the walk and the decode read the same staged payload");
+
+// Sum of the sizes of chunks [0, c), c <= kFusedMaxChunks, from the header
+// table: 16-byte units of eight sizes, then the last few sizes, by a warp.
+__device__ __forceinline__ uint32_t header_sum_before(const DecodeArgs &p, uint32_t c, uint32_t lane) {
+  const uint4 *h4 = reinterpret_cast<const uint4 *>(p.in);
+  const uint32_t u1 = c / 8;
+  uint32_t part = 0;
+  for (uint32_t i = lane; i < u1; i += 32) part += (uint32_t)sum8_sizes(__ldg(h4 + i));
+  if (lane < (c & 7u)) part += __ldg(reinterpret_cast<const uint16_t *>(p.in) + 8u * u1 + lane);
+  return __reduce_add_sync(0xFFFFFFFFu, part);
+}
 
 template <bool W16>
 __global__ void __launch_bounds__(kFusedWarps * 32, 6)
@@ -1072,12 +1090,12 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 6)
   __shared__ __align__(16) uint32_t stage[kFusedWarps][kStageWords];  // per warp: the chunk's payload
   __shared__ uint16_t starts[kFusedWarps][32];  // start bit of block b >= 1
   __shared__ __align__(8) unsigned long long mbar[kFusedWarps];
-  griddep_wait();  // the group sums are complete
+  griddep_wait();  // a previous kernel of the stream is complete
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t C = p.num_chunks;
   const uint32_t c = blockIdx.x * kFusedWarps + warp;
   if (c >= C) return;
-  const uint64_t off = 2ull * C + sizes_before_chunk(p, c, lane);
+  const uint64_t off = 2ull * C + header_sum_before(p, c, lane);
   const uint32_t L = __ldg(reinterpret_cast<const uint16_t *>(p.in) + c);
   const uint32_t raw_len = (uint32_t)umin64(4096u, p.nbytes - (uint64_t)c * 4096u);
   if (L == 0 || L > raw_len || off + L > p.comp_bytes) {
@@ -1138,6 +1156,7 @@ uint32_t coop_max_chunks() { return kCoopMaxChunks; }
 int coop_warps() { return kCoopWarps; }
 size_t coop_smem_bytes() { return kCoopSmem; }
 int fused_warps() { return kFusedWarps; }
+uint32_t fused_max_chunks() { return kFusedMaxChunks; }
 const void *walk_decode_kernel_ptr(bool w16) {
   return w16 ? reinterpret_cast<const void *>(&walk_decode_kernel<true>)
              : reinterpret_cast<const void *>(&walk_decode_kernel<false>);

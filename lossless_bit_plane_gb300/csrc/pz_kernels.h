@@ -55,6 +55,7 @@ int coop_warps();                     // chunks per cooperative-walk block (one 
 size_t coop_smem_bytes();
 const void *walk_coop_kernel_ptr(bool w16);
 int fused_warps();                    // chunks per fused walk-and-decode block (one warp each)
+uint32_t fused_max_chunks();          // the fused kernel's limit on C (its header sums are 32-bit)
 const void *walk_decode_kernel_ptr(bool w16);  // small inputs: walk and decode in one launch
 const void *size_sum_kernel_ptr();    // 256 threads, one block per group but the last
 int decode_threads();

@@ -59,17 +59,3 @@ def explain_mismatch(data, ew: int, got: bytes, want: bytes) -> str:
             return (msg + f"first differing chunk {c}: L gpu {gl} oracle {int(w_l[c])}; "
                     f"oracle tags {tags.tolist()} bits {bits.tolist()}")
     return msg + "headers and payloads equal"
-
-
-def sampled_chunk_parity(data: np.ndarray, ew: int, stream: bytes, chunks) -> None:
-    """Chunks are independent: the oracle's stream for one chunk's bytes is
-    its header followed by its payload, which must equal the GPU stream's."""
-    n = data.size
-    lens, offs = chunk_table(stream, n)
-    raw = data.view(np.uint8)
-    for c in chunks:
-        piece = raw[4096 * c: min(n, 4096 * c + 4096)].tobytes()
-        ref = oracle.compress(piece, ew)
-        L = int(lens[c])
-        assert ref[:2] == int(L).to_bytes(2, "little"), (c, L, ref[:2])
-        assert stream[offs[c]: offs[c] + L] == ref[2:], f"chunk {c} payload differs"

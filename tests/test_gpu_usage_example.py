@@ -1,5 +1,6 @@
-"""The README's Python example, run as written (through the C ABI), so that the
-documented usage stays correct."""
+"""The Python usage example given to users of the library (compress,
+decompress, sampled sizes, swap out and in), run as written through the C
+ABI, so that the documented usage stays correct."""
 import pytest
 
 pytestmark = pytest.mark.gpu
@@ -7,7 +8,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-def test_readme_example():
+def test_usage_example():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     from lossless_bit_plane_gb300 import _lib, build
 

@@ -57,6 +57,15 @@ WORKED = [
     (bytes(128), 4, {0: 32, 1: 39, 2: 7, 3: 32, 4: 1024}, 2),
     # all-zero BF16: BX one run code of 16 planes (6); DBX 16 + 6
     (bytes(128), 2, {0: 64, 1: 22, 2: 6, 3: 64, 4: 1024}, 2),
+    # BF16 s_0 = 1, rest 0: BX run15 (6) + single one (11) = 17; DBX = base 16
+    # + the 17th (borrow) plane, d_1 = -1 mod 2^17, Gray code bit 16 alone:
+    # single one q = 0 (11) + run of the 16 planes below (6) = 33; ZBX = mask
+    # 64 + run15 (6) + the 1-bit plane, verbatim in 2 bits = 72
+    (u16([1] + [0] * 63), 2, {0: 80, 1: 33, 2: 17, 3: 72, 4: 1024}, 2),
+    # s_k = rotl(0x0F0F0F0F, (k-3) mod 8): every BX plane verbatim (32 x 33),
+    # DBX 32 + 32 + 3 + 31 x 32 (its plane 31 is the only zero plane); RAW wins
+    (u32([0xE1E1E1E1, 0xC3C3C3C3, 0x87878787, 0x0F0F0F0F, 0x1E1E1E1E, 0x3C3C3C3C, 0x78787878,
+          0xF0F0F0F0] * 4), 4, {0: 1056, 1: 1059, 2: 1056, 3: 1088, 4: 1024}, 4),
 ]
 
 

@@ -64,6 +64,22 @@ def test_noalloc_matches_pz_compress_on_calls_in_a_row():
         assert got == want
 
 
+def test_noalloc_at_its_maximum_size():
+    # nbytes == PZ_NOALLOC_MAX_BYTES: 65,536 chunks, so the look-back words
+    # and the ticket fill the static scratch array to its last word; then a
+    # ragged input just below the maximum, and the maximum again (each call
+    # finds the previous call's contents in the array).
+    rng = np.random.default_rng(37)
+    n = _lib.NOALLOC_MAX_BYTES
+    full = _dev(W.relu_values(n // 4, rng))
+    assert full.numel() == n
+    ragged = full[: n - 4096 + 100]
+    for x, ew in ((full, 4), (ragged, 2), (full, 4)):
+        want = _reference(x, ew)
+        got = _noalloc(x, ew)
+        assert got == want
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     FAKE = 0x100000  # never dereferenced: the size checks come first
     n = _lib.NOALLOC_MAX_BYTES + 1
