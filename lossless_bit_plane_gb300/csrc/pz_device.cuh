@@ -1,8 +1,7 @@
 // pz_device.cuh — device helpers shared by the encoder and decoder kernels:
-// inline-PTX wrappers (mbarrier, TMA tile load, relaxed global atomics-free
-// loads/stores, byte permute), SWAR helpers for two 16-bit symbols per
-// 32-bit word, a 32x32 bit-matrix transpose, and an LSB-first bit writer into
-// shared memory.
+// inline-PTX wrappers (mbarrier, TMA tile load, relaxed global loads/stores,
+// shared memory by 32-bit address, byte permute), SWAR helpers for two
+// 16-bit symbols per 32-bit word and a 32x32 bit-matrix transpose.
 #pragma once
 
 #include <cstdint>
@@ -92,63 +91,40 @@ __device__ __forceinline__ void transpose32(uint32_t (&a)[32]) {
   }
 }
 
-// ------------------------------------------------------- bit writer (smem)
-// LSB-first writer into a zeroed shared-memory word buffer. Words that may be
-// shared with a neighbouring writer (the first and the last) and all others
-// alike are written with atomicOr, so writers may start at any bit.
-struct BitWriter {
-  uint32_t *buf;
-  uint32_t widx;
-  uint32_t nacc;
-  uint32_t cap;  // words in buf; writes at or past it are dropped
-  uint64_t acc;
-  __device__ __forceinline__ void init(uint32_t *b, uint32_t bitpos, uint32_t cap_words) {
-    buf = b;
-    widx = bitpos >> 5;
-    nacc = bitpos & 31u;
-    cap = cap_words;
-    acc = 0;
-  }
-  // n <= 32 and v < 2^n
-  __device__ __forceinline__ void put(uint32_t v, uint32_t n) {
-    acc |= (uint64_t)v << nacc;
-    nacc += n;
-    if (nacc >= 32) {
-      if (widx < cap) atomicOr(&buf[widx], (uint32_t)acc);
-      ++widx;
-      acc >>= 32;
-      nacc -= 32;
-    }
-  }
-  // n <= 33 and v < 2^n (one or two words may complete)
-  __device__ __forceinline__ void put_wide(uint64_t v, uint32_t n) {
-    acc |= v << nacc;
-    nacc += n;
-    if (nacc >= 32) {
-      if (widx < cap) atomicOr(&buf[widx], (uint32_t)acc);
-      ++widx;
-      acc >>= 32;
-      nacc -= 32;
-      if (nacc >= 32) {
-        if (widx < cap) atomicOr(&buf[widx], (uint32_t)acc);
-        ++widx;
-        acc >>= 32;
-        nacc -= 32;
-      }
-    }
-  }
-  __device__ __forceinline__ void put64(uint64_t v, uint32_t n) {  // n <= 64
-    if (n > 32) {
-      put((uint32_t)v, 32);
-      put((uint32_t)(v >> 32), n - 32);
-    } else {
-      put((uint32_t)v, n);
-    }
-  }
-  __device__ __forceinline__ void flush() {
-    if (nacc && widx < cap) atomicOr(&buf[widx], (uint32_t)acc);
-  }
-};
+// --------------------------------------- shared memory by 32-bit address
+// Accesses by a shared-window address (smem_u32 of a pointer), so that row
+// and swizzle arithmetic stays in 32-bit registers.
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 q;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+               : "r"(addr)
+               : "memory");
+  return q;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
+}
+// *addr |= v as one shared-memory reduction (no value returned)
+__device__ __forceinline__ void ors32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 // --------------------------------------------- programmatic dependent launch
 // A kernel launched with the programmatic-serialization attribute right after
