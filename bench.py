@@ -561,13 +561,15 @@ def run_sizes(args, segs, d_in, totals_host, dev, stream):
     return {"size_only": size_only, "ablation": ablation}
 
 
-def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=64 << 20):
-    """Outside the headline's timed region: the compressed swap path
-    (pz_swap_out / pz_swap_in, 64 MiB pieces, pinned host memory) on a few
-    segments, against the plain pinned copy of the same bytes over the host
-    link, with the paper's Equation 2 evaluated on the measured numbers:
-    x_t = min(m/g, max(m/(c g), m/B)) with g the plain copy's rate, c the
-    ratio and B the codec's rate on that segment (raw bytes / kernel time)."""
+def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=64 << 20, slot=4 << 20):
+    """Outside the headline's timed region: the compressed swap path on a few
+    segments (a first piece of 32 MiB, then pieces of 64 MiB;
+    pinned host memory), into one host buffer (pz_swap_out / pz_swap_in) and
+    into a pool of 4 MiB host slots (pz_pool_*), against the plain pinned copy
+    of the same bytes over the host link, with the paper's Equation 2
+    evaluated on the measured numbers: x_t = min(m/g, max(m/(c g), m/B)) with
+    g the plain copy's rate, c the ratio and B the codec's rate on that
+    segment (raw bytes / kernel time)."""
     import torch
 
     from lossless_bit_plane_gb300 import _lib
@@ -580,6 +582,7 @@ def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=64 << 20):
     nmax = max(segs[i].nbytes for i in pick)
     h_raw = torch.empty(nmax, dtype=torch.uint8).pin_memory()
     bufs = _lib.SwapBuffers(nmax, piece, dev)
+    pool = _lib.SwapPool(_lib.pz_swap_capacity(nmax, piece) + 2 * slot + (1 << 20), slot, piece, dev)
     back = torch.empty(nmax, dtype=torch.uint8, device=dev)
 
     def wall(fn, reps=3):
@@ -591,6 +594,10 @@ def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=64 << 20):
         torch.cuda.synchronize()
         return (time.perf_counter() - t0) / reps
 
+    def pool_out(x, ew):
+        t, _ = pool.swap_out(x, ew)
+        pool.release(t)
+
     rows = []
     for i in pick:
         t, x = segs[i], d_in[i]
@@ -601,15 +608,25 @@ def run_swap(segs, d_in, totals_host, t_c, t_d, dev, stream, piece=64 << 20):
         s_out = n / wall(lambda: bufs.swap_out(x, t.elem_width)) / 1e9
         s_in = n / wall(lambda: bufs.swap_in(length, back[:n])) / 1e9
         ok = int(bufs.status.item()) == 0 and torch.equal(back[:n], x)
+        p_out = n / wall(lambda: pool_out(x, t.elem_width)) / 1e9
+        tensor, stored = pool.swap_out(x, t.elem_width)
+        p_in = n / wall(lambda: pool.swap_in(tensor, back[:n])) / 1e9
+        ok = ok and int(pool.status.item()) == 0 and torch.equal(back[:n], x)
+        pool.release(tensor)
         c = n / totals_host[i]
         b_c, b_d = n / (t_c[i] * 1e-3) / 1e9, n / (t_d[i] * 1e-3) / 1e9
         eq2 = lambda g, b: 1.0 / min(1.0 / g, max(1.0 / (c * g), 1.0 / b))  # noqa: E731  (GB/s of raw bytes)
-        rows.append({"segment": t.name, "ratio": round(c, 4), "container_bytes": length,
+        e_out, e_in = eq2(g_out, b_c), eq2(g_in, b_d)
+        rows.append({"segment": t.name, "ratio": round(c, 4), "container_bytes": length, "pool_stored_bytes": stored,
                      "link_d2h_gbs": round(g_out, 1), "link_h2d_gbs": round(g_in, 1),
                      "swap_out_gbs": round(s_out, 1), "swap_in_gbs": round(s_in, 1),
-                     "eq2_out_gbs": round(eq2(g_out, b_c), 1), "eq2_in_gbs": round(eq2(g_in, b_d), 1),
+                     "pool_swap_out_gbs": round(p_out, 1), "pool_swap_in_gbs": round(p_in, 1),
+                     "eq2_out_gbs": round(e_out, 1), "eq2_in_gbs": round(e_in, 1),
+                     "swap_out_of_eq2": round(s_out / e_out, 3), "swap_in_of_eq2": round(s_in / e_in, 3),
+                     "swap_out_of_link": round(s_out / g_out, 3), "swap_in_of_link": round(s_in / g_in, 3),
                      "round_trip_exact": ok})
-    return {"piece_bytes": piece, "unit": "GB/s of raw bytes", "host_memory": "pinned", "segments": rows}
+    return {"max_piece_bytes": piece, "pool_slot_bytes": slot, "unit": "GB/s of raw bytes",
+            "host_memory": "pinned", "segments": rows}
 
 
 def count_launches(step) -> int:

@@ -169,17 +169,25 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width,
  * link work at the same time (Section III-A: the engine compresses
  * device-to-host swaps and decompresses host-to-device ones; Section III-C,
  * Equation 2: a transfer is limited by the link or by the engine, whichever
- * is slower). The tensor is cut into pieces of piece_bytes (a multiple of
- * 4096); piece k+1 is coded on `stream` while piece k is on the link (an
- * internal copy stream of the call). Host memory should be pinned for the
- * copies to overlap (pageable memory works, serialised). These calls block
- * the host (the sizes of the pieces are needed on the host) and cannot be
- * captured in a CUDA graph.
+ * is slower, and the runtime bypasses the engine when compression would not
+ * shorten the transfer). The tensor is cut into pieces of at most
+ * piece_bytes (a multiple of 4096): a first piece of half that size (so
+ * that the first step, which nothing overlaps, is shorter), then pieces of
+ * piece_bytes. Piece k+1 is coded on `stream` while piece k is on the link
+ * (an internal copy stream). A piece whose stream would not be shorter than its bytes is
+ * moved raw. Host memory should be pinned for the copies to overlap
+ * (pageable memory works, serialised).
  *
- * Container written by pz_swap_out (little-endian): a 32-byte head (u32
- * "PZSW", u32 pieces, u64 nbytes, u64 piece_bytes, u32 elem_width, u32 0),
- * one u64 stream length per piece, then each piece's pz_compress stream,
- * each starting at a 16-byte boundary.
+ * Container (little-endian): a 32-byte head (u32 "PZS2", u32 pieces n, u64
+ * nbytes, u64 piece_bytes, u32 elem_width, u32 0), n entries of 16 bytes
+ * (u64 raw bytes of the piece; u64 stored bytes, bit 63 set when the piece
+ * is stored raw), then each piece -- its pz_compress stream, or its bytes --
+ * at a 16-byte boundary.
+ *
+ * Swap-out blocks the host until the container is complete (each piece's
+ * stored length is needed on the host to copy it). Swap-in only enqueues:
+ * the host bytes must stay unchanged until `stream` has completed the call.
+ * Calls that share d_work must be ordered on the same stream.
  * ---------------------------------------------------------------------- */
 
 /* Device staging bytes both calls need for piece_bytes (0 if piece_bytes is
@@ -187,8 +195,9 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width,
  * encoder's scratch. Host-only, pure. */
 size_t pz_swap_work_bytes(size_t piece_bytes);
 
-/* Host bytes pz_swap_out may write for nbytes in pieces of piece_bytes
- * (0 for an invalid piece size). Host-only, pure. */
+/* Host bytes pz_swap_out may write for nbytes in pieces of at most
+ * piece_bytes (0 for an invalid piece size): the head and table plus every
+ * piece's raw bytes rounded up to 16. Host-only, pure. */
 size_t pz_swap_capacity(size_t nbytes, size_t piece_bytes);
 
 /* Swap out nbytes at d_in (device, 16-byte aligned) into the container at
@@ -204,14 +213,59 @@ pz_status pz_swap_out(const void *d_in, size_t nbytes, int elem_width,
 
 /* Swap in: decode the container of h_bytes at h_in (host) back into nbytes
  * at d_out (device, 16-byte aligned). The container's head must match
- * nbytes and its piece lengths must lie inside h_bytes (else PZ_ERR_ARG,
+ * nbytes and its table must be consistent with h_bytes (else PZ_ERR_ARG,
  * nothing enqueued). d_work as for pz_swap_out with the container's piece
- * size. Returns once the copies are done and the decodes are enqueued on
- * `stream`; *d_status (device int) becomes PZ_OK or PZ_ERR_CORRUPT when
- * the stream completes. */
+ * size. Returns once the copies and decodes are enqueued on `stream`;
+ * *d_status (device int) becomes PZ_OK or PZ_ERR_CORRUPT when the stream
+ * completes. */
 pz_status pz_swap_in(const void *h_in, size_t h_bytes, void *d_work,
                      size_t work_bytes, void *d_out, size_t nbytes,
                      int *d_status, pz_stream_t stream);
+
+/* A pool of fixed-size host slots for swapped tensors (Section III-A: on the
+ * host, compressed tensors occupy fixed-size chunks of a pinned pool, so
+ * that their variable sizes do not fragment the allocator). A swapped
+ * tensor's container is laid over a chain of slots (container byte x in the
+ * (x / slot_bytes)-th slot of the chain); its handle is the index of its
+ * first slot. The pool lives in host memory the caller provides (pinned for
+ * the copies to overlap) and keeps all its state there; calls on one pool
+ * are thread-safe. */
+typedef struct pz_pool_s pz_pool;
+
+/* Host bytes of a pool of nslots slots of slot_bytes (a multiple of 4096):
+ * the pool's head and slot links, then the slots, 4096-aligned. 0 for an
+ * invalid size. Host-only, pure. */
+size_t pz_pool_bytes(size_t slot_bytes, size_t nslots);
+
+/* Lay a pool out in h_mem (host, 64-byte aligned, `bytes` long; as many
+ * slots as fit). *pool points into h_mem; the pool needs no teardown
+ * beyond freeing h_mem once no call uses it. Errors: PZ_ERR_ARG,
+ * PZ_ERR_CAPACITY (not one slot fits). */
+pz_status pz_pool_init(void *h_mem, size_t bytes, size_t slot_bytes,
+                       pz_pool **pool);
+
+/* Slots not held by a swapped tensor. */
+size_t pz_pool_free_slots(pz_pool *pool);
+
+/* pz_swap_out into slots of the pool: *tensor (host) = the handle, and
+ * *stored_bytes (host, may be NULL) = the container's length. The head and
+ * piece table must fit in one slot (PZ_ERR_ARG otherwise). PZ_ERR_CAPACITY
+ * when the pool runs out of slots (the slots taken are given back).
+ * Other arguments and errors as pz_swap_out. */
+pz_status pz_pool_swap_out(pz_pool *pool, const void *d_in, size_t nbytes,
+                           int elem_width, size_t piece_bytes, void *d_work,
+                           size_t work_bytes, unsigned int *tensor,
+                           size_t *stored_bytes, pz_stream_t stream);
+
+/* pz_swap_in of a tensor of the pool; the tensor keeps its slots (release
+ * them once `stream` has completed the call). Arguments and errors as
+ * pz_swap_in. */
+pz_status pz_pool_swap_in(pz_pool *pool, unsigned int tensor, void *d_work,
+                          size_t work_bytes, void *d_out, size_t nbytes,
+                          int *d_status, pz_stream_t stream);
+
+/* Give a tensor's slots back to the pool. PZ_ERR_ARG for a bad handle. */
+pz_status pz_pool_release(pz_pool *pool, unsigned int tensor);
 
 /* Largest input pz_compress_noalloc accepts: 256 MiB (65,536 chunks). */
 #define PZ_NOALLOC_MAX_BYTES ((size_t)256 << 20)

@@ -2,8 +2,8 @@
 
 The functions mirror the C ABI in ``include/planezip.h`` one to one
 (``pz_max_compressed_bytes``, ``pz_compress``, ``pz_decompress``,
-``pz_compress_candidates``, ``pz_compressed_size``, the swap path ``pz_swap_*`` and
-``pz_compress_noalloc``); every step
+``pz_compress_candidates``, ``pz_compressed_size``, the swap path ``pz_swap_*``, the
+host slot pool ``pz_pool_*`` and ``pz_compress_noalloc``); every step
 of the codec runs in the library's CUDA kernels. The ``*_tensor`` helpers
 below use PyTorch only to allocate device memory and to name the current
 stream. There is no fallback: if the library is missing or cannot be loaded,
@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "PZ_OK", 1: "PZ_ERR_ARG", 2: "PZ_ERR_CAPACITY", 3: "PZ_ERR_CO
                 4: "PZ_ERR_CUDA", 5: "PZ_ERR_TIMEOUT"}
 EXPORTS = ("pz_max_compressed_bytes", "pz_compress", "pz_decompress", "pz_compress_candidates",
            "pz_compressed_size", "pz_swap_work_bytes", "pz_swap_capacity", "pz_swap_out", "pz_swap_in",
-           "pz_test_lookback_timeout", "pz_compress_noalloc")
+           "pz_pool_bytes", "pz_pool_init", "pz_pool_free_slots", "pz_pool_swap_out", "pz_pool_swap_in",
+           "pz_pool_release", "pz_test_lookback_timeout", "pz_compress_noalloc")
 # candidate masks (bit t = tag t: ZVC 0, DBX 1, BX 2, ZBX 3, raw 4; raw is always allowed)
 PZ_CAND_ZVC, PZ_CAND_DBX, PZ_CAND_BX, PZ_CAND_ZBX, PZ_CAND_RAW = 0x01, 0x02, 0x04, 0x08, 0x10
 PZ_CAND_ALL = 0x1F
@@ -66,6 +67,20 @@ def load() -> ctypes.CDLL:
         L.pz_swap_out.restype = ctypes.c_int
         L.pz_swap_in.argtypes = [vp, sz, vp, sz, vp, sz, vp, vp]
         L.pz_swap_in.restype = ctypes.c_int
+        u32 = ctypes.c_uint
+        L.pz_pool_bytes.argtypes = [sz, sz]
+        L.pz_pool_bytes.restype = sz
+        L.pz_pool_init.argtypes = [vp, sz, sz, ctypes.POINTER(vp)]
+        L.pz_pool_init.restype = ctypes.c_int
+        L.pz_pool_free_slots.argtypes = [vp]
+        L.pz_pool_free_slots.restype = sz
+        L.pz_pool_swap_out.argtypes = [vp, vp, sz, ctypes.c_int, sz, vp, sz, ctypes.POINTER(u32), ctypes.POINTER(sz),
+                                       vp]
+        L.pz_pool_swap_out.restype = ctypes.c_int
+        L.pz_pool_swap_in.argtypes = [vp, u32, vp, sz, vp, sz, vp, vp]
+        L.pz_pool_swap_in.restype = ctypes.c_int
+        L.pz_pool_release.argtypes = [vp, u32]
+        L.pz_pool_release.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -136,6 +151,40 @@ def pz_swap_in(h_in: int, h_bytes: int, d_work: int, work_bytes: int, d_out: int
                stream: int = 0) -> int:
     return int(load().pz_swap_in(h_in or None, h_bytes, d_work or None, work_bytes, d_out or None, nbytes,
                                  d_status or None, stream or None))
+
+
+def pz_pool_bytes(slot_bytes: int, nslots: int) -> int:
+    return int(load().pz_pool_bytes(slot_bytes, nslots))
+
+
+def pz_pool_init(h_mem: int, nbytes: int, slot_bytes: int) -> tuple[int, int]:
+    """Returns (status, pool handle as an integer address)."""
+    pool = ctypes.c_void_p(0)
+    rc = load().pz_pool_init(h_mem or None, nbytes, slot_bytes, ctypes.byref(pool))
+    return int(rc), int(pool.value or 0)
+
+
+def pz_pool_free_slots(pool: int) -> int:
+    return int(load().pz_pool_free_slots(pool or None))
+
+
+def pz_pool_swap_out(pool: int, d_in: int, nbytes: int, elem_width: int, piece_bytes: int, d_work: int,
+                     work_bytes: int, stream: int = 0) -> tuple[int, int, int]:
+    """Returns (status, tensor handle, stored container bytes)."""
+    tensor, stored = ctypes.c_uint(0), ctypes.c_size_t(0)
+    rc = load().pz_pool_swap_out(pool or None, d_in or None, nbytes, elem_width, piece_bytes, d_work or None,
+                                 work_bytes, ctypes.byref(tensor), ctypes.byref(stored), stream or None)
+    return int(rc), int(tensor.value), int(stored.value)
+
+
+def pz_pool_swap_in(pool: int, tensor: int, d_work: int, work_bytes: int, d_out: int, nbytes: int, d_status: int,
+                    stream: int = 0) -> int:
+    return int(load().pz_pool_swap_in(pool or None, tensor, d_work or None, work_bytes, d_out or None, nbytes,
+                                      d_status or None, stream or None))
+
+
+def pz_pool_release(pool: int, tensor: int) -> int:
+    return int(load().pz_pool_release(pool or None, tensor))
 
 
 # ---------------------------------------------------------------- torch glue
@@ -248,3 +297,51 @@ class SwapBuffers:
         if rc != PZ_OK:
             raise PlaneZipError("pz_swap_in", rc)
         return self.status
+
+
+class SwapPool:
+    """A pool of fixed-size slots in pinned host memory (torch allocation)
+    that swapped tensors occupy, and the device staging the swaps need; the
+    pool's bookkeeping and the swaps run in the library."""
+
+    def __init__(self, pool_bytes: int, slot_bytes: int = 4 << 20, piece_bytes: int = 64 << 20, device="cuda"):
+        import torch
+
+        self.piece_bytes = piece_bytes
+        self.work_bytes = pz_swap_work_bytes(piece_bytes)
+        if self.work_bytes == 0:
+            raise ValueError("piece_bytes must be a positive multiple of 4096")
+        self.work = torch.empty(self.work_bytes, dtype=torch.uint8, device=device)
+        self.host = torch.empty(pool_bytes + 64, dtype=torch.uint8).pin_memory()
+        base = (self.host.data_ptr() + 63) // 64 * 64
+        rc, self.pool = pz_pool_init(base, pool_bytes, slot_bytes)
+        if rc != PZ_OK:
+            raise PlaneZipError("pz_pool_init", rc)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def free_slots(self) -> int:
+        return pz_pool_free_slots(self.pool)
+
+    def swap_out(self, x, elem_width: int) -> tuple[int, int]:
+        """(tensor handle, stored bytes); blocks until the tensor is in the pool."""
+        rc, tensor, stored = pz_pool_swap_out(self.pool, x.data_ptr(), x.numel() * x.element_size(), elem_width,
+                                              self.piece_bytes, self.work.data_ptr(), self.work_bytes,
+                                              _current_stream_handle(x.device))
+        if rc != PZ_OK:
+            raise PlaneZipError("pz_pool_swap_out", rc)
+        return tensor, stored
+
+    def swap_in(self, tensor: int, out):
+        """Decode a pooled tensor into ``out`` (asynchronous); returns the
+        device status tensor. Release the tensor after the stream is done."""
+        rc = pz_pool_swap_in(self.pool, tensor, self.work.data_ptr(), self.work_bytes, out.data_ptr(),
+                             out.numel() * out.element_size(), self.status.data_ptr(),
+                             _current_stream_handle(out.device))
+        if rc != PZ_OK:
+            raise PlaneZipError("pz_pool_swap_in", rc)
+        return self.status
+
+    def release(self, tensor: int) -> None:
+        rc = pz_pool_release(self.pool, tensor)
+        if rc != PZ_OK:
+            raise PlaneZipError("pz_pool_release", rc)

@@ -80,17 +80,36 @@ def test_candidates_and_size_argument_errors_are_host_side(lib):
     assert size(FAKE_IN + 4, n, 4, _lib.PZ_CAND_ALL, 1, 0, FAKE_WORD) == _lib.PZ_ERR_ARG  # misaligned
 
 
+def piece_schedule(n, P):
+    """The documented piece schedule: a first piece of half of P (rounded
+    down to 4096, at least 4096), then pieces of P, the last possibly
+    shorter."""
+    out, rem, s = [], n, max(4096, (P // 2) // 4096 * 4096)
+    while rem:
+        out.append(min(s, rem))
+        rem -= out[-1]
+        s = P
+    return out
+
+
+def test_piece_schedule_examples():
+    M = 1 << 20
+    assert piece_schedule(128 * M, 64 * M) == [32 * M, 64 * M, 32 * M]
+    assert piece_schedule(10 * M, 64 * M) == [10 * M]
+    assert piece_schedule(3 << 20, 1 << 20) == [M // 2, M, M, M // 2]
+    assert piece_schedule(12288, 4096) == [4096] * 3
+    assert sum(piece_schedule(300_001, 65536)) == 300_001
+
+
 def test_swap_sizes_closed_forms(lib):
     assert _lib.pz_swap_work_bytes(0) == 0 and _lib.pz_swap_work_bytes(4097) == 0
     for piece in (4096, 1 << 20, 16 << 20):
         stage = (_lib.pz_max_compressed_bytes(piece) + 15) // 16 * 16
         assert _lib.pz_swap_work_bytes(piece) == 2 * stage + 32
-    for n, piece in ((0, 4096), (1, 4096), (4096, 4096), (4097, 4096), (10 << 20, 1 << 20), (3 << 20, 2 << 20)):
-        k = (n + piece - 1) // piece
-        cap = (32 + 8 * k + 15) // 16 * 16
-        for i in range(k):
-            raw = min(piece, n - i * piece)
-            cap += (2 * ((raw + 4095) // 4096) + raw + 15) // 16 * 16
+    for n, piece in ((0, 4096), (1, 4096), (4096, 4096), (4097, 4096), (10 << 20, 1 << 20), (3 << 20, 2 << 20),
+                     (128 << 20, 32 << 20), (300_001, 65536), (10 << 20, 64 << 20)):
+        sizes = piece_schedule(n, piece)
+        cap = (32 + 16 * len(sizes) + 15) // 16 * 16 + sum((r + 15) // 16 * 16 for r in sizes)
         assert _lib.pz_swap_capacity(n, piece) == cap
 
 
@@ -111,25 +130,51 @@ def test_swap_argument_and_container_errors_are_host_side(lib):
     # an empty tensor needs no device at all: the container is its head
     rc, total = _lib.pz_swap_out(0, 0, 4, piece, 0, 0, h, cap)
     assert rc == _lib.PZ_OK and total == 32
-    assert struct.unpack_from("<IIQQII", host.raw, 0) == (0x57535A50, 0, 0, piece, 4, 0)
-    # swap-in rejects a container that does not match, before any device work
-    # a well-formed container of three 1 KB piece streams (>= 2 bytes per chunk of a 1 MiB piece)
-    head = struct.pack("<IIQQII", 0x57535A50, 3, n, piece, 4, 0) + struct.pack("<3Q", 1024, 1024, 1024)
+    assert struct.unpack_from("<IIQQII", host.raw, 0) == (0x32535A50, 0, 0, piece, 4, 0)
+    # swap-in rejects a container that does not match, before any device work:
+    # a well-formed container of three 1 MiB pieces, each a 1 KB stream
+    head = struct.pack("<IIQQII", 0x32535A50, 3, n, piece, 4, 0) + struct.pack("<6Q", piece, 1024, piece, 1024,
+                                                                               piece, 1024)
     ctypes.memmove(h, head, len(head))
-    ok_len = 64 + 3 * 1024
+    ok_len = 80 + 3 * 1024
     assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n + 1, FAKE_WORD) == _lib.PZ_ERR_ARG   # nbytes
     assert _lib.pz_swap_in(h, 40, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG          # truncated
-    bad = struct.pack("<IIQQII", 0x57535A51, 3, n, piece, 4, 0)
+    bad = struct.pack("<IIQQII", 0x57535A50, 3, n, piece, 4, 0)
     ctypes.memmove(h, bad, len(bad))
     assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG      # magic
     ctypes.memmove(h, head, len(head))
-    ctypes.memmove(h + 32, struct.pack("<Q", 1 << 40), 8)                                            # length
-    assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG
-    ctypes.memmove(h + 32, struct.pack("<Q", 511), 8)                                                # < 2C
-    assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG
-    ctypes.memmove(h + 32, struct.pack("<Q", 1024), 8)
+    for entry in ((piece, 1 << 40), (piece, 511), (piece, piece), (piece + 4096, 1024), (0, 1024),
+                  (piece, (1 << 63) | 1024), (piece - 4096, 1024)):
+        ctypes.memmove(h + 32, struct.pack("<2Q", *entry), 16)                         # bad lengths or sizes
+        assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG, entry
+    ctypes.memmove(h + 32, struct.pack("<2Q", piece, 1024), 16)
     assert _lib.pz_swap_in(h, ok_len - 1, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG  # past the end
     assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work - 1, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_CAPACITY
+
+
+def test_pool_layout_and_host_side_errors(lib):
+    import ctypes
+
+    S = 1 << 20
+    assert _lib.pz_pool_bytes(S, 0) == 0 and _lib.pz_pool_bytes(4095, 4) == 0
+    # the head (40 bytes of fields and a mutex) and 4-byte slot links, then the
+    # slots from a 4096-byte boundary
+    assert _lib.pz_pool_bytes(S, 3) == 4096 + 3 * S
+    assert _lib.pz_pool_bytes(S, 1024) == 8192 + 1024 * S
+    mem = ctypes.create_string_buffer(_lib.pz_pool_bytes(65536, 5) + 64)
+    base = (ctypes.addressof(mem) + 63) // 64 * 64
+    assert _lib.pz_pool_init(base + 8, len(mem) - 64, 65536)[0] == _lib.PZ_ERR_ARG       # alignment
+    assert _lib.pz_pool_init(base, 4096 + 65535, 65536)[0] == _lib.PZ_ERR_CAPACITY        # no slot fits
+    rc, pool = _lib.pz_pool_init(base, len(mem) - 64, 65536)
+    assert rc == _lib.PZ_OK and pool == base
+    assert _lib.pz_pool_free_slots(pool) == 5
+    assert _lib.pz_pool_release(pool, 5) == _lib.PZ_ERR_ARG                               # no such slot
+    assert _lib.pz_pool_swap_out(pool, FAKE_IN, 4096, 0, 65536, FAKE_OUT, 1 << 30)[0] == _lib.PZ_ERR_ARG
+    assert _lib.pz_pool_swap_in(pool, 7, FAKE_OUT, 1 << 30, FAKE_IN, 4096, FAKE_WORD) == _lib.PZ_ERR_ARG
+    # an empty tensor takes one slot (its head) and gives it back
+    rc, t, stored = _lib.pz_pool_swap_out(pool, 0, 0, 4, 65536, 0, 0)
+    assert rc == _lib.PZ_OK and stored == 32 and _lib.pz_pool_free_slots(pool) == 4
+    assert _lib.pz_pool_release(pool, t) == _lib.PZ_OK and _lib.pz_pool_free_slots(pool) == 5
 
 
 def test_timeout_hook_argument_errors_are_host_side(lib):

@@ -26,7 +26,7 @@ def test_usage_example():
     assert sizes.numel() == (C + 3) // 4
     headers = out[: 2 * C].cpu().view(torch.int16).to(torch.int32) & 0xFFFF
     assert torch.equal(sizes.cpu(), headers[::4])
-    swap = _lib.SwapBuffers(x.numel() * 4)                 # 64 MiB pieces by default
+    swap = _lib.SwapBuffers(x.numel() * 4)                 # pieces of at most 64 MiB by default
     length = swap.swap_out(x, 4)                           # compressed container in pinned host memory
     back.zero_()
     status = swap.swap_in(length, back)                    # back on the device
