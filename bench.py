@@ -48,10 +48,10 @@ WORKLOAD = ("1 GiB throughput sweep: {ReLU, smooth conv, causal attention} x {FP
 # until the encoder is captured again. It is also null when the sweep's
 # dominant call is not the encoder.
 NCU_ENCODER_TRAFFIC = {
-    "sources": ("lossless_bit_plane_gb300/csrc/encode.cu", "lossless_bit_plane_gb300/csrc/pz_device.cuh",
-                "lossless_bit_plane_gb300/csrc/pz_format.cuh"),
-    "sources_sha256": "0ae8796a719666857273a4e5ef7b7131b1f7fb92ac0dfb35576670d19c9c25b1",
-    "bytes_per_launch": 208.32e6,
+    "sources": ("lossless_bit_plane_gb300/csrc/encode.cu", "lossless_bit_plane_gb300/csrc/pz_encode_block.cuh",
+                "lossless_bit_plane_gb300/csrc/pz_device.cuh", "lossless_bit_plane_gb300/csrc/pz_format.cuh"),
+    "sources_sha256": "9b85898e5342fd02388c0d97d75f686c7f2a305b909450730538efcad1540ed4",
+    "bytes_per_launch": 211.10e6,
 }
 
 
