@@ -264,7 +264,9 @@ pz_status pz_pool_swap_in(pz_pool *pool, unsigned int tensor, void *d_work,
                           size_t work_bytes, void *d_out, size_t nbytes,
                           int *d_status, pz_stream_t stream);
 
-/* Give a tensor's slots back to the pool. PZ_ERR_ARG for a bad handle. */
+/* Give a tensor's slots back to the pool (after every call that uses them
+ * has completed on its stream). PZ_ERR_ARG for a handle that is not a
+ * swapped tensor's, including one already released. */
 pz_status pz_pool_release(pz_pool *pool, unsigned int tensor);
 
 /* Largest input pz_compress_noalloc accepts: 256 MiB (65,536 chunks). */

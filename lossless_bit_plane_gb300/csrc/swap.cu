@@ -517,6 +517,14 @@ pz_status pz_pool_swap_in(pz_pool *pool, unsigned int tensor, void *d_work, size
 
 pz_status pz_pool_release(pz_pool *pool, unsigned int tensor) {
   if (!pool || pool->magic != kPoolMagic || tensor >= pool->nslots) return PZ_ERR_ARG;
+  {  // a tensor's first slot starts with its container's head; clearing it
+     // makes a second release of the same handle an error
+    std::lock_guard<std::mutex> lk(pool->mu);
+    uint32_t magic = 0;
+    std::memcpy(&magic, pool->slot(tensor), 4);
+    if (magic != kMagic) return PZ_ERR_ARG;
+    std::memset(pool->slot(tensor), 0, 4);
+  }
   pool_release_chain(pool, tensor);
   return PZ_OK;
 }

@@ -175,6 +175,13 @@ def test_pool_layout_and_host_side_errors(lib):
     rc, t, stored = _lib.pz_pool_swap_out(pool, 0, 0, 4, 65536, 0, 0)
     assert rc == _lib.PZ_OK and stored == 32 and _lib.pz_pool_free_slots(pool) == 4
     assert _lib.pz_pool_release(pool, t) == _lib.PZ_OK and _lib.pz_pool_free_slots(pool) == 5
+    assert _lib.pz_pool_release(pool, t) == _lib.PZ_ERR_ARG and _lib.pz_pool_free_slots(pool) == 5  # twice
+    ts = [_lib.pz_pool_swap_out(pool, 0, 0, 2, 65536, 0, 0)[1] for _ in range(5)]
+    assert sorted(ts) == list(range(5)) and _lib.pz_pool_free_slots(pool) == 0
+    assert _lib.pz_pool_swap_out(pool, 0, 0, 2, 65536, 0, 0)[0] == _lib.PZ_ERR_CAPACITY  # no slot left
+    for t in ts:
+        assert _lib.pz_pool_release(pool, t) == _lib.PZ_OK
+    assert _lib.pz_pool_free_slots(pool) == 5
 
 
 def test_timeout_hook_argument_errors_are_host_side(lib):

@@ -29,6 +29,17 @@ def test_usage_example():
     swap = _lib.SwapBuffers(x.numel() * 4)                 # pieces of at most 64 MiB by default
     length = swap.swap_out(x, 4)                           # compressed container in pinned host memory
     back.zero_()
-    status = swap.swap_in(length, back)                    # back on the device
+    status = swap.swap_in(length, back)                    # back on the device (asynchronous)
     torch.cuda.synchronize()
     assert int(status.item()) == 0 and torch.equal(back.view(torch.float32), x)
+
+    pool = _lib.SwapPool(64 << 20, slot_bytes=1 << 20)     # 64 MiB of pinned host slots
+    free = pool.free_slots()
+    handle, stored = pool.swap_out(x, 4)                   # the tensor occupies ceil(stored / 1 MiB) slots
+    assert free - pool.free_slots() == (stored + (1 << 20) - 1) // (1 << 20)
+    back.zero_()
+    status = pool.swap_in(handle, back)
+    torch.cuda.synchronize()
+    pool.release(handle)
+    assert int(status.item()) == 0 and torch.equal(back.view(torch.float32), x)
+    assert pool.free_slots() == free
