@@ -134,16 +134,18 @@ constexpr int kOutWords = 1024 + 4;
 constexpr int kOutPad = 4;  // readable words before a warp's output buffer (copy_out reads from word -4)
 
 // Shared memory per warp: one 4 KB stage buffer (1024-aligned, the TMA
-// destination), the chunk's output word buffer, an mbarrier (16 bytes
-// reserved). One stage at three CTAs per SM (24 warps): the next chunk is
-// loaded after this one is done, and the other warps cover that load's
-// latency. (A second stage, with the next chunk's load in flight, needs more
-// shared memory than three CTAs allow.)
+// destination), the chunk's output region, an mbarrier (16 bytes reserved).
+// The output region is 128-byte aligned: before emission it holds the
+// lanes' DBX rows (lane l's at byte 128 l), then the output word buffer
+// from byte 16 (word 0) on. One stage at three CTAs per SM (24 warps): the
+// next chunk is loaded after this one is done, and the other warps cover
+// that load's latency. (A second stage, with the next chunk's load in
+// flight, needs more shared memory than three CTAs allow.)
 template <bool W16>
 struct EncCfg {
   static constexpr int kMinCtas = 3;
   static constexpr size_t kStageBytes = 4096;
-  static constexpr size_t kOutBytes = (kOutPad + kOutWords) * 4;
+  static constexpr size_t kOutBytes = ((kOutPad + kOutWords) * 4 + 127) / 128 * 128;
   static constexpr size_t kBytes = 1024 + kEncWarps * kStageBytes + kEncWarps * kOutBytes + kEncWarps * 16;
 };
 
@@ -175,8 +177,9 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *st = base + warp * Cfg::kStageBytes;
-  uint32_t *outbuf =
-      reinterpret_cast<uint32_t *>(base + kEncWarps * Cfg::kStageBytes + warp * Cfg::kOutBytes) + kOutPad;
+  uint8_t *outreg = base + kEncWarps * Cfg::kStageBytes + warp * Cfg::kOutBytes;  // 128-byte aligned
+  uint32_t *outbuf = reinterpret_cast<uint32_t *>(outreg) + kOutPad;
+  const uint32_t drow = smem_u32(outreg) + lane * 128u;  // this lane's DBX row (until emission)
   uint64_t *mbar = reinterpret_cast<uint64_t *>(base + kEncWarps * Cfg::kStageBytes + kEncWarps * Cfg::kOutBytes) +
                    2 * warp;
   const uint32_t mb = smem_u32(mbar);
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     const bool active = lane < nblk;
 
     const uint32_t rowbase = smem_u32(st) + lane * 128u;
-    Sizes z = W16 ? classify16(rowbase, lane, p.candidates) : classify32(rowbase, lane, p.candidates);
+    Sizes z = W16 ? classify16(rowbase, lane, p.candidates, drow) : classify32(rowbase, lane, p.candidates, drow);
     const uint32_t tag = z.tag;
     uint32_t bits = z.bits;
     bits = active ? bits + 3 : 0;
@@ -288,6 +291,11 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
     if (lane == 0) st_relaxed_u64(p.status + t, (t == 0 ? kFlagInc : kFlagAgg) | L);
 
     if (!raw_chunk) {
+      // planes first (the DBX rows lie in the output buffer), then the
+      // buffer is cleared and the codes go in
+      Prep pr{0u, 0u};
+      if (active) pr = W16 ? prep16(tag, z.m0, z.m1, rowbase, lane, drow) : prep32(tag, z.m0, rowbase, lane, drow);
+      __syncwarp();
       const uint32_t nw = (L + 3) / 4 + 1;
       for (uint32_t i = lane; i < nw; i += 32) outbuf[i] = 0;
       __syncwarp();
@@ -297,10 +305,9 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
         wr.put(tag, 3);
         const Plan &pl = z.win;
         if (W16)
-          emit16(wr, tag, z.m0, z.m1, rowbase, lane, pl, z.bp);
+          emit16(wr, tag, z.m0, z.m1, rowbase, lane, pl, z.bp, pr);
         else
-          emit32(wr, tag, z.m0, rowbase, lane, pl, z.bp);
-
+          emit32(wr, tag, z.m0, rowbase, lane, pl, z.bp, pr);
       }
     } else {
       for (uint32_t u = lane; u < 256; u += 32)

@@ -152,18 +152,28 @@ __device__ __forceinline__ void load_block(uint32_t rowbase, uint32_t lane, uint
   for (int j = 0; j < 32; ++j) s[j] = W16 ? split_word(raw, j) : raw[j];
 }
 
+// The lane's row of DBX words: 32 words in a 128-byte-aligned row, 16-byte
+// units swizzled like a stage row (unit u at u ^ (lane & 7)). The classifier
+// leaves there, as it streams the block, the Gray-coded deltas that DBX codes
+// (word 0: zero, the base is coded verbatim), so that emission takes them as
+// they are instead of deriving them again.
+__device__ __forceinline__ uint32_t drow_unit(uint32_t drow, uint32_t lane, uint32_t u) {  // u < 8
+  return row_swz(drow, lane) ^ (u << 4);
+}
+
 // ------------------------------------------------------------ FP32 classify
 // s: the block's 32 symbols. Returns the five candidate sizes (tag excluded).
 // The words are streamed from the stage row four at a time, so that only the
-// accumulators stay in registers.
-__device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uint32_t cand) {
+// accumulators stay in registers; DBX's Gray-coded deltas go to the lane's
+// DBX row (drow) unit by unit.
+__device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uint32_t cand, uint32_t drow) {
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0;  // BX
   uint32_t nz = 0, zn = 0, adjz = 0, last = 0;                            // ZBX / ZVC
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Bw = 0, gdprev = 0;  // DBX
   uint32_t xprev = 0;
   // word k of the block; the loop runs over 16-byte units (4 words each) so
   // that the kernel's code stays small
-  auto step = [&](uint32_t x, uint32_t k) {
+  auto step = [&](uint32_t x, uint32_t k) -> uint32_t {
     const uint32_t g = x ^ (x >> 1);
     ors |= x;
     c |= b & g;
@@ -177,6 +187,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
     zn |= ~g & m;  // some survivor has a 0 in the plane
     adjz |= last & g;
     last = x ? g : last;
+    uint32_t gdk = 0;
     if (k) {
       const uint64_t d = (uint64_t)x - (uint64_t)xprev;
       const uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);  // hi: borrow mask
@@ -189,23 +200,23 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
       if (k > 1) adjd |= gdprev & gd;
       andd &= gd;
       gdprev = gd;
+      gdk = gd;
     }
     xprev = x;
+    return gdk;
   };
   {
     const uint4 q = stage_unit(rowbase, lane, 0);
     step(q.x, 0);
-    step(q.y, 1);
-    step(q.z, 2);
-    step(q.w, 3);
+    const uint32_t d1 = step(q.y, 1), d2 = step(q.z, 2), d3 = step(q.w, 3);
+    sts128(drow_unit(drow, lane, 0), 0u, d1, d2, d3);
   }
 #pragma unroll 1
   for (uint32_t u = 1; u < 8; ++u) {
     const uint4 q = stage_unit(rowbase, lane, u);
-    step(q.x, 4 * u);
-    step(q.y, 4 * u + 1);
-    step(q.z, 4 * u + 2);
-    step(q.w, 4 * u + 3);
+    const uint32_t d0 = step(q.x, 4 * u), d1 = step(q.y, 4 * u + 1), d2 = step(q.z, 4 * u + 2),
+                   d3 = step(q.w, 4 * u + 3);
+    sts128(drow_unit(drow, lane, u), d0, d1, d2, d3);
   }
   Bw >>= 1;  // borrow of delta k at bit k-1
   Sizes z;
@@ -245,8 +256,9 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
 // ------------------------------------------------------------ BF16 classify
 // sp: split-packed block (word j = symbol j | symbol j+32 << 16).
 // Split-packed words (word j = symbol j | symbol j+32 << 16) are built while
-// streaming the stage row: word j needs raw words j/2 and 16 + j/2.
-__device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uint32_t cand) {
+// streaming the stage row: word j needs raw words j/2 and 16 + j/2. DBX's
+// Gray-coded deltas, split-packed the same way, go to the lane's DBX row.
+__device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uint32_t cand, uint32_t drow) {
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0, g0 = 0;
   uint32_t mlo = 0, mhi = 0, zn = 0, adjz = 0, last = 0, fst = 0, seen = 0;
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Blo = 0, Bhi = 0, gdprev = 0,
@@ -255,7 +267,7 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
   uint32_t xprev = 0;
   // split-packed word j >= 1 (symbols j and j+32); the loop below runs over
   // half 16-byte units (4 words each) so that the kernel's code stays small
-  auto step = [&](uint32_t x, uint32_t j) {
+  auto step = [&](uint32_t x, uint32_t j) -> uint32_t {
     const uint32_t g = x ^ ((x >> 1) & 0x7FFF7FFFu);
     ors |= x;
     c |= b & g;
@@ -286,6 +298,7 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     Blo = __funnelshift_r(Blo, bo >> 15, 1);  // d_j's borrow ends at bit j (shifted to j-1 below)
     Bhi = __funnelshift_l(bo, Bhi, 1);        // d_{j+32}'s borrow enters at bit 0 (reversed below)
     xprev = x;
+    return gd;
   };
   {
     const uint4 qa = stage_unit(rowbase, lane, 0), qb = stage_unit(rowbase, lane, 4);
@@ -317,19 +330,21 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     Blo = 0;  // d_32's borrow (bo bit 31) goes to plane position 31 after the loop
     d32b = bo;
     xprev = x;
-    step(prmt(qa.x, qb.x, 0x7632u), 1);
-    step(prmt(qa.y, qb.y, 0x5410u), 2);
-    step(prmt(qa.y, qb.y, 0x7632u), 3);
+    const uint32_t d1 = step(prmt(qa.x, qb.x, 0x7632u), 1);
+    const uint32_t d2 = step(prmt(qa.y, qb.y, 0x5410u), 2);
+    const uint32_t d3 = step(prmt(qa.y, qb.y, 0x7632u), 3);
+    sts128(drow_unit(drow, lane, 0), gd, d1, d2, d3);
   }
 #pragma unroll 1
   for (uint32_t h = 1; h < 8; ++h) {
     const uint4 qa = stage_unit(rowbase, lane, h >> 1), qb = stage_unit(rowbase, lane, 4u + (h >> 1));
     const bool hi = (h & 1u) != 0;
     const uint32_t a0 = hi ? qa.z : qa.x, a1 = hi ? qa.w : qa.y, b0 = hi ? qb.z : qb.x, b1 = hi ? qb.w : qb.y;
-    step(prmt(a0, b0, 0x5410u), 4u * h);
-    step(prmt(a0, b0, 0x7632u), 4u * h + 1u);
-    step(prmt(a1, b1, 0x5410u), 4u * h + 2u);
-    step(prmt(a1, b1, 0x7632u), 4u * h + 3u);
+    const uint32_t d0 = step(prmt(a0, b0, 0x5410u), 4u * h);
+    const uint32_t d1 = step(prmt(a0, b0, 0x7632u), 4u * h + 1u);
+    const uint32_t d2 = step(prmt(a1, b1, 0x5410u), 4u * h + 2u);
+    const uint32_t d3 = step(prmt(a1, b1, 0x7632u), 4u * h + 3u);
+    sts128(drow_unit(drow, lane, h), d0, d1, d2, d3);
   }
   // the accumulations above left word j's bits at j (low halves) or 31 - j
   // (high halves); bring them to the plane positions the masks use
@@ -589,9 +604,57 @@ __device__ __forceinline__ void emit_plane_codes(PosWriter &wr, uint32_t rowbase
   }
 }
 
-// FP32 emit of the chosen candidate. nz: non-zero symbol mask.
+// Planes of the kept candidate, before anything is written to the output
+// buffer (the DBX rows lie in it): the candidate's words -- DBX's
+// Gray-coded deltas from the lane's DBX row, the block's words (BX) or its
+// survivors compacted in place (ZBX) from the stage row, Gray-coded here --
+// go through one 32x32 bit transpose into the stage row as plane rows
+// (store_planes). Every lane runs the same loads, from a row picked by its
+// candidate. Returns the plane width W (0: no plane codes) and, for DBX,
+// the base symbol, read before the stage row is overwritten.
+struct Prep {
+  uint32_t W;
+  uint32_t base;
+};
+
+__device__ __forceinline__ Prep prep32(uint32_t tag, uint32_t nz, uint32_t rowbase, uint32_t lane, uint32_t drow) {
+  Prep pr{0u, 0u};
+  if (tag == kTagRAW || tag == kTagZVC || (tag == kTagZBX && nz == 0)) return pr;
+  const bool dbx = (tag == kTagDBX);
+  pr.base = lds32(stage_word(rowbase, lane, 0));
+  pr.W = dbx ? 31u : 32u;
+  if (tag == kTagZBX) {
+    uint32_t cnt = 0;  // compact the survivors in place (cnt <= k)
+    for (uint32_t m = nz; m; m &= m - 1, ++cnt)
+      sts32(stage_word(rowbase, lane, cnt), lds32(stage_word(rowbase, lane, __ffs(m) - 1)));
+    pr.W = cnt;
+  }
+  // DBX rows are Gray-coded already (row bit j = delta j, bit 0 zero)
+  const uint32_t src = dbx ? drow : rowbase, gmask = dbx ? 0u : 0xFFFFFFFFu;
+  uint32_t T[32];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 q = lds128(row_swz(src, lane) ^ ((uint32_t)u << 4));
+    T[4 * u] = q.x;
+    T[4 * u + 1] = q.y;
+    T[4 * u + 2] = q.z;
+    T[4 * u + 3] = q.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) T[j] ^= (T[j] >> 1) & gmask;
+  transpose32(T);
+  if (pr.W < 32u && !dbx) {  // ZBX: plane bits past the survivors come from stale words
+    const uint32_t keep = (1u << pr.W) - 1u;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) T[i] &= keep;
+  }
+  store_planes(rowbase, lane, T);
+  return pr;
+}
+
+// FP32 emit of the chosen candidate after prep32. nz: non-zero symbol mask.
 __device__ __forceinline__ void emit32(PosWriter &wr, uint32_t tag, uint32_t nz, uint32_t rowbase, uint32_t lane,
-                                      const Plan &pl, uint64_t bp) {
+                                      const Plan &pl, uint64_t bp, const Prep &pr) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) wr.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -602,49 +665,63 @@ __device__ __forceinline__ void emit32(PosWriter &wr, uint32_t tag, uint32_t nz,
     for (uint32_t m = nz; m; m &= m - 1) wr.put(lds32(stage_word(rowbase, lane, __ffs(m) - 1)), 32);
     return;
   }
-  uint32_t T[32];
-  uint64_t topv = 0;
-  int W = 32;
-  if (tag == kTagZBX) {
-    if (nz == 0) return;
-    uint32_t cnt = 0;  // compact the survivors in place (cnt <= k)
-    for (uint32_t m = nz; m; m &= m - 1, ++cnt)
-      sts32(stage_word(rowbase, lane, cnt), lds32(stage_word(rowbase, lane, __ffs(m) - 1)));
-    W = (int)cnt;
-  }
-  {
-    load_block<false>(rowbase, lane, T);  // BX, DBX and the compacted ZBX row
-    if (tag == kTagDBX) {  // deltas (33 bits: bit 32 is the borrow), Gray-coded; the borrow plane came from classify
-      wr.put(T[0], 32);
-      uint32_t prev = T[0];
-      T[0] = 0;
-#pragma unroll
-      for (int j = 1; j < 32; ++j) {
-        const uint32_t cur = T[j];
-        const uint64_t d = (uint64_t)cur - (uint64_t)prev;
-        const uint32_t lo = (uint32_t)d, hi = (uint32_t)(d >> 32);
-        T[j] = lo ^ __funnelshift_r(lo, hi, 1);
-        prev = cur;
-      }
-      topv = bp;
-      W = 31;
-    } else {  // BX, or ZBX over its first W (compacted) words
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t t = (j < W) ? T[j] : 0u;
-        T[j] = t ^ (t >> 1);
-      }
-    }
-  }
-  transpose32(T);
-  store_planes(rowbase, lane, T);
-  emit_plane_codes<false>(wr, rowbase, lane, W, (int)ceil_log2_u32((uint32_t)W), tag == kTagDBX, topv, pl);
+  if (pr.W == 0) return;  // ZBX without survivors: the mask alone
+  const bool dbx = (tag == kTagDBX);
+  if (dbx) wr.put(pr.base, 32);
+  emit_plane_codes<false>(wr, rowbase, lane, (int)pr.W, (int)ceil_log2_u32(pr.W), dbx, dbx ? bp : 0ull, pl);
 }
 
-// BF16 emit of the chosen candidate. mlo/mhi: non-zero masks of symbols
-// 0..31 / 32..63.
+// BF16 planes of the kept candidate (as prep32): split-packed words (word j
+// = symbol j | symbol j+32 << 16) -- DBX's from its row as they are, the
+// others built from the raw or compacted row.
+__device__ __forceinline__ Prep prep16(uint32_t tag, uint32_t mlo, uint32_t mhi, uint32_t rowbase, uint32_t lane,
+                                      uint32_t drow) {
+  Prep pr{0u, 0u};
+  if (tag == kTagRAW || tag == kTagZVC || (tag == kTagZBX && (mlo | mhi) == 0)) return pr;
+  const bool dbx = (tag == kTagDBX);
+  pr.base = lds16(stage_half(rowbase, lane, 0));
+  pr.W = dbx ? 63u : 64u;
+  if (tag == kTagZBX) {
+    uint32_t cnt = 0;  // compact the survivors' half-words in place (cnt <= h)
+    for (uint32_t m = mlo; m; m &= m - 1, ++cnt)
+      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, __ffs(m) - 1)));
+    for (uint32_t m = mhi; m; m &= m - 1, ++cnt)
+      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, 31 + __ffs(m))));
+    pr.W = cnt;
+  }
+  const uint32_t src = dbx ? drow : rowbase, gmask = dbx ? 0u : 0x7FFF7FFFu;
+  uint32_t R[32], T[32];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 q = lds128(row_swz(src, lane) ^ ((uint32_t)u << 4));
+    R[4 * u] = q.x;
+    R[4 * u + 1] = q.y;
+    R[4 * u + 2] = q.z;
+    R[4 * u + 3] = q.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t t = dbx ? R[j] : split_word(R, j);
+    T[j] = t ^ ((t >> 1) & gmask);
+  }
+  transpose32(T);  // T[i] = plane i of symbols 0..31, T[16 + i] = plane i of symbols 32..63
+  if (pr.W < 64u && !dbx) {  // ZBX: plane bits past the survivors come from stale half-words
+    const uint32_t keep_lo = (pr.W >= 32u) ? 0xFFFFFFFFu : ((1u << pr.W) - 1u);
+    const uint32_t keep_hi = (pr.W <= 32u) ? 0u : ((1u << (pr.W - 32u)) - 1u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      T[i] &= keep_lo;
+      T[16 + i] &= keep_hi;
+    }
+  }
+  store_planes(rowbase, lane, T);
+  return pr;
+}
+
+// BF16 emit of the chosen candidate after prep16. mlo/mhi: non-zero masks of
+// symbols 0..31 / 32..63.
 __device__ __forceinline__ void emit16(PosWriter &wr, uint32_t tag, uint32_t mlo, uint32_t mhi, uint32_t rowbase,
-                                      uint32_t lane, const Plan &pl, uint64_t bp) {
+                                      uint32_t lane, const Plan &pl, uint64_t bp, const Prep &pr) {
   if (tag == kTagRAW) {
 #pragma unroll 4
     for (uint32_t k = 0; k < 32; ++k) wr.put(lds32(stage_word(rowbase, lane, k)), 32);
@@ -659,49 +736,10 @@ __device__ __forceinline__ void emit16(PosWriter &wr, uint32_t tag, uint32_t mlo
     for (uint32_t m = mhi; m; m &= m - 1) wr.put(lds16(stage_half(rowbase, lane, 31 + __ffs(m))), 16);
     return;
   }
-  uint32_t T[32];
-  uint64_t topv = 0;
-  int W = 64;
-  if (tag == kTagZBX) {
-    uint32_t cnt = 0;  // compact the survivors' half-words in place (cnt <= h)
-    for (uint32_t m = mlo; m; m &= m - 1, ++cnt)
-      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, __ffs(m) - 1)));
-    for (uint32_t m = mhi; m; m &= m - 1, ++cnt)
-      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, 31 + __ffs(m))));
-    if (cnt == 0) return;
-    W = (int)cnt;
-  }
-  {
-    load_block<true>(rowbase, lane, T);  // BX, DBX and the compacted ZBX row
-    if (tag == kTagDBX) {  // deltas (17 bits: bit 16 is the borrow), Gray-coded; the borrow plane came from classify
-      wr.put(T[0] & 0xFFFFu, 16);
-      uint32_t prev = T[31] << 16;  // word 0: no delta for s_0 (the base); d_32 = s_32 - s_31
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t cur = T[j];
-        uint32_t bo;
-        uint32_t d = sub16x2(cur, prev, bo);
-        if (j == 0) {
-          d &= 0xFFFF0000u;
-          bo &= 0x80000000u;
-        }
-        T[j] = d ^ (((d >> 1) & 0x7FFF7FFFu) | bo);
-        prev = cur;
-      }
-      topv = bp;
-      W = 63;
-    } else {  // BX, or ZBX over its first W (compacted) half-words
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t keep = ((j < W) ? 0x0000FFFFu : 0u) | ((j + 32 < W) ? 0xFFFF0000u : 0u);
-        const uint32_t t = T[j] & keep;
-        T[j] = t ^ ((t >> 1) & 0x7FFF7FFFu);
-      }
-    }
-  }
-  transpose32(T);
-  store_planes(rowbase, lane, T);
-  emit_plane_codes<true>(wr, rowbase, lane, W, (int)ceil_log2_u32((uint32_t)W), tag == kTagDBX, topv, pl);
+  if (pr.W == 0) return;  // ZBX without survivors: the masks alone
+  const bool dbx = (tag == kTagDBX);
+  if (dbx) wr.put(pr.base, 16);
+  emit_plane_codes<true>(wr, rowbase, lane, (int)pr.W, (int)ceil_log2_u32(pr.W), dbx, dbx ? bp : 0ull, pl);
 }
 
 }  // namespace pz
