@@ -450,7 +450,8 @@ struct PosWriter {
     if (sh + len > 32u) ors32(a + 4, __funnelshift_l(v, 0u, sh));
     pos += len;
   }
-  // 33 <= len <= 64 bits: lo = bits 0..31, hi = bits 32..len-1
+  // len <= 64 bits: lo = bits 0..31, hi = bits 32..len-1 (zero when len <=
+  // 32; the second reduction then ORs in only what spills past the word)
   __device__ __forceinline__ void put_wide(uint32_t lo, uint32_t hi, uint32_t len) {
     const uint32_t sh = pos & 31u, a = word_addr();
     ors32(a, lo << sh);
@@ -487,17 +488,14 @@ struct PosWriter {
     if (sh > 28u) ors32(a + 20, __funnelshift_l(c4, 0u, sh));
     pos += 132;
   }
-  // the verbatim codes of four planes of 31 bits (FP32 DBX), given as rows
-  // whose bit 0 is zero (row = X << 1): 128 bits, row | 1 each
-  __device__ __forceinline__ void put_verbatim31x4(uint32_t R3, uint32_t R2, uint32_t R1, uint32_t R0) {
-    const uint32_t c0 = R3 | 1u, c1 = R2 | 1u, c2 = R1 | 1u, c3 = R0 | 1u;
-    const uint32_t sh = pos & 31u, a = word_addr();
-    ors32(a, c0 << sh);
-    ors32(a + 4, __funnelshift_l(c0, c1, sh));
-    ors32(a + 8, __funnelshift_l(c1, c2, sh));
-    ors32(a + 12, __funnelshift_l(c2, c3, sh));
-    if (sh) ors32(a + 16, __funnelshift_l(c3, 0u, sh));
-    pos += 128;
+  // the verbatim codes of four planes of W <= 31 bits (FP32 DBX, ZBX), each
+  // 1 + W bits given as its code word c = 1 | X << 1: two pairs of codes, each
+  // pair at most 64 bits
+  __device__ __forceinline__ void put_verbatim_pairs(uint32_t c3, uint32_t c2, uint32_t c1, uint32_t c0, uint32_t W) {
+    const uint32_t s = W + 1u;
+    const uint64_t A = (uint64_t)c3 | ((uint64_t)c2 << s), B = (uint64_t)c1 | ((uint64_t)c0 << s);
+    put_wide((uint32_t)A, (uint32_t)(A >> 32), 2u * s);
+    put_wide((uint32_t)B, (uint32_t)(B >> 32), 2u * s);
   }
 };
 
@@ -532,8 +530,9 @@ __device__ __forceinline__ void put_short(PosWriter &wr, int i, uint32_t below_n
 // four, the group's rows brought by one 16-byte load (BF16: two, the low and
 // the high 32 symbols), every lane of the warp at the same group. For DBX a
 // row's bit j is delta j, so plane bit q = delta q+1 is the row shifted by
-// one. A verbatim plane takes the first branch -- four at once for FP32 BX
-// and DBX blocks whose whole group is verbatim, as the low planes of
+// one. A verbatim plane takes the first branch -- four at once for FP32
+// blocks whose whole group is verbatim (BX: five words of codes; DBX and
+// ZBX, at most 31 bits a plane: two pairs of codes), as the low planes of
 // activations are in whole warps -- and every other code (a zero run at its
 // top plane, a 5-bit code, a position code) the second; zero planes below a
 // run's top plane emit nothing. Each path exists once in the code (rolled
@@ -577,11 +576,14 @@ __device__ __forceinline__ void emit_plane_codes(PosWriter &wr, uint32_t rowbase
     uint4 qa = lds128(plane_unit(rowbase, lane, (uint32_t)g));
     uint4 qb = make_uint4(0, 0, 0, 0);
     if (W16) qb = lds128(plane_unit(rowbase, lane, (uint32_t)g + 4u));
-    if (!W16 && gv == 15u && (dbx || W == 32)) {  // four verbatim planes of 31 (DBX) or 32 bits
-      if (dbx)
-        wr.put_verbatim31x4(qa.w, qa.z, qa.y, qa.x);
-      else
+    if (!W16 && gv == 15u) {  // four verbatim planes: 32 bits (BX) or at most 31 (DBX, ZBX)
+      if (W == 32) {
         wr.put_verbatim32x4(qa.w, qa.z, qa.y, qa.x);
+      } else {  // a DBX row is X << 1 already
+        const uint32_t sh1 = dbx ? 0u : 1u;
+        wr.put_verbatim_pairs((qa.w << sh1) | 1u, (qa.z << sh1) | 1u, (qa.y << sh1) | 1u, (qa.x << sh1) | 1u,
+                              (uint32_t)W);
+      }
       continue;
     }
     // planes 4g+3 .. 4g: the rows move down one place per step (the top row in .w)
