@@ -488,6 +488,34 @@ struct PosWriter {
     if (sh > 28u) ors32(a + 20, __funnelshift_l(c4, 0u, sh));
     pos += 132;
   }
+  // N whole words (len bits, the last word possibly partial), B[0] first
+  template <int N>
+  __device__ __forceinline__ void put_words(const uint32_t (&B)[N], uint32_t len) {
+    const uint32_t sh = pos & 31u, a = word_addr();
+    ors32(a, B[0] << sh);
+#pragma unroll
+    for (int k = 1; k < N; ++k) ors32(a + 4u * (uint32_t)k, __funnelshift_l(B[k - 1], B[k], sh));
+    if (sh + len > 32u * (uint32_t)N) ors32(a + 4u * (uint32_t)N, __funnelshift_l(B[N - 1], 0u, sh));
+    pos += len;
+  }
+  // the verbatim codes of four BF16 planes of 64 bits (X = hi:lo), X3 first:
+  // 4 x 65 bits, nine words before the shift to the position
+  __device__ __forceinline__ void put_verbatim64x4(uint32_t l3, uint32_t h3, uint32_t l2, uint32_t h2, uint32_t l1,
+                                                   uint32_t h1, uint32_t l0, uint32_t h0) {
+    // code k = 1 | X << 1 as three words e0, e1, e2 (e2 one bit)
+    auto e0 = [](uint32_t l) { return (l << 1) | 1u; };
+    auto e1 = [](uint32_t l, uint32_t h) { return __funnelshift_l(l, h, 1); };
+    const uint32_t B[9] = {e0(l3),
+                           e1(l3, h3),
+                           (h3 >> 31) | (e0(l2) << 1),
+                           __funnelshift_l(e0(l2), e1(l2, h2), 1),
+                           __funnelshift_l(e1(l2, h2), h2 >> 31, 1) | (e0(l1) << 2),
+                           __funnelshift_l(e0(l1), e1(l1, h1), 2),
+                           __funnelshift_l(e1(l1, h1), h1 >> 31, 2) | (e0(l0) << 3),
+                           __funnelshift_l(e0(l0), e1(l0, h0), 3),
+                           __funnelshift_l(e1(l0, h0), h0 >> 31, 3)};
+    put_words<9>(B, 260u);
+  }
   // the verbatim codes of four planes of W <= 31 bits (FP32 DBX, ZBX), each
   // 1 + W bits given as its code word c = 1 | X << 1: two pairs of codes, each
   // pair at most 64 bits
@@ -530,10 +558,11 @@ __device__ __forceinline__ void put_short(PosWriter &wr, int i, uint32_t below_n
 // four, the group's rows brought by one 16-byte load (BF16: two, the low and
 // the high 32 symbols), every lane of the warp at the same group. For DBX a
 // row's bit j is delta j, so plane bit q = delta q+1 is the row shifted by
-// one. A verbatim plane takes the first branch -- four at once for FP32
-// blocks whose whole group is verbatim (BX: five words of codes; DBX and
-// ZBX, at most 31 bits a plane: two pairs of codes), as the low planes of
-// activations are in whole warps -- and every other code (a zero run at its
+// one. A verbatim plane takes the first branch -- four at once where the
+// block's whole group is verbatim (FP32 BX: five words of codes; FP32 DBX
+// and ZBX, at most 31 bits a plane: two pairs of codes; BF16 BX: nine words;
+// BF16 DBX: eight; BF16 ZBX: four codes of at most 64 bits), as the low
+// planes of activations are in whole warps -- and every other code (a zero run at its
 // top plane, a 5-bit code, a position code) the second; zero planes below a
 // run's top plane emit nothing. Each path exists once in the code (rolled
 // loops), which keeps the kernel's instructions within the instruction
@@ -576,6 +605,21 @@ __device__ __forceinline__ void emit_plane_codes(PosWriter &wr, uint32_t rowbase
     uint4 qa = lds128(plane_unit(rowbase, lane, (uint32_t)g));
     uint4 qb = make_uint4(0, 0, 0, 0);
     if (W16) qb = lds128(plane_unit(rowbase, lane, (uint32_t)g + 4u));
+    if (W16 && gv == 15u) {  // four verbatim BF16 planes
+      if (dbx) {  // 63 bits: a row pair is X << 1, so each code is the pair | 1, 64 bits
+        const uint32_t B[8] = {qa.w | 1u, qb.w, qa.z | 1u, qb.z, qa.y | 1u, qb.y, qa.x | 1u, qb.x};
+        wr.put_words<8>(B, 256u);
+      } else if (W == 64) {
+        wr.put_verbatim64x4(qa.w, qb.w, qa.z, qb.z, qa.y, qb.y, qa.x, qb.x);
+      } else {  // ZBX, at most 63 bits: one code of at most 64 bits each
+        const uint32_t s = (uint32_t)W + 1u;
+        wr.put_wide((qa.w << 1) | 1u, __funnelshift_l(qa.w, qb.w, 1), s);
+        wr.put_wide((qa.z << 1) | 1u, __funnelshift_l(qa.z, qb.z, 1), s);
+        wr.put_wide((qa.y << 1) | 1u, __funnelshift_l(qa.y, qb.y, 1), s);
+        wr.put_wide((qa.x << 1) | 1u, __funnelshift_l(qa.x, qb.x, 1), s);
+      }
+      continue;
+    }
     if (!W16 && gv == 15u) {  // four verbatim planes: 32 bits (BX) or at most 31 (DBX, ZBX)
       if (W == 32) {
         wr.put_verbatim32x4(qa.w, qa.z, qa.y, qa.x);
