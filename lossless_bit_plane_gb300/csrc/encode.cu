@@ -296,8 +296,8 @@ __global__ void __launch_bounds__(kEncWarps * 32, EncCfg<W16>::kMinCtas)
       Prep pr{0u, 0u};
       if (active) pr = W16 ? prep16(tag, z.m0, z.m1, rowbase, lane, drow) : prep32(tag, z.m0, rowbase, lane, drow);
       __syncwarp();
-      const uint32_t nw = (L + 3) / 4 + 1;
-      for (uint32_t i = lane; i < nw; i += 32) outbuf[i] = 0;
+      const uint32_t nu = ((L + 3) / 4 + 4) / 4;  // 16-byte units covering the stream's words and one more
+      for (uint32_t i = lane; i < nu; i += 32) reinterpret_cast<uint4 *>(outbuf)[i] = make_uint4(0, 0, 0, 0);
       __syncwarp();
       if (active) {
         PosWriter wr;

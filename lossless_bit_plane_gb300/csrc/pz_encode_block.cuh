@@ -652,8 +652,9 @@ __device__ __forceinline__ void emit_plane_codes(PosWriter &wr, uint32_t rowbase
 
 // Planes of the kept candidate, before anything is written to the output
 // buffer (the DBX rows lie in it): the candidate's words -- DBX's
-// Gray-coded deltas from the lane's DBX row, the block's words (BX) or its
-// survivors compacted in place (ZBX) from the stage row, Gray-coded here --
+// Gray-coded deltas from the lane's DBX row, the block's words (BX) from the
+// stage row, or its survivors (ZBX), stored in order at their ranks into the
+// lane's DBX row, which ZBX does not need, Gray-coded here --
 // go through one 32x32 bit transpose into the stage row as plane rows
 // (store_planes). Every lane runs the same loads, from a row picked by its
 // candidate. Returns the plane width W (0: no plane codes) and, for DBX,
@@ -669,14 +670,22 @@ __device__ __forceinline__ Prep prep32(uint32_t tag, uint32_t nz, uint32_t rowba
   const bool dbx = (tag == kTagDBX);
   pr.base = lds32(stage_word(rowbase, lane, 0));
   pr.W = dbx ? 31u : 32u;
-  if (tag == kTagZBX) {
-    uint32_t cnt = 0;  // compact the survivors in place (cnt <= k)
-    for (uint32_t m = nz; m; m &= m - 1, ++cnt)
-      sts32(stage_word(rowbase, lane, cnt), lds32(stage_word(rowbase, lane, __ffs(m) - 1)));
-    pr.W = cnt;
+  if (tag == kTagZBX) {  // the survivors, in order, to the lane's DBX row (which ZBX does not use)
+    const uint32_t dx = row_swz(drow, lane);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 q = stage_unit(rowbase, lane, (uint32_t)u);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = 4 * u + k;
+        if (nz & (1u << j)) sts32(dx ^ ((uint32_t)__popc(nz & ((1u << j) - 1u)) << 2), w[k]);
+      }
+    }
+    pr.W = (uint32_t)__popc(nz);
   }
   // DBX rows are Gray-coded already (row bit j = delta j, bit 0 zero)
-  const uint32_t src = dbx ? drow : rowbase, gmask = dbx ? 0u : 0xFFFFFFFFu;
+  const uint32_t src = (tag == kTagBX) ? rowbase : drow, gmask = dbx ? 0u : 0xFFFFFFFFu;
   uint32_t T[32];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
@@ -717,9 +726,10 @@ __device__ __forceinline__ void emit32(PosWriter &wr, uint32_t tag, uint32_t nz,
   emit_plane_codes<false>(wr, rowbase, lane, (int)pr.W, (int)ceil_log2_u32(pr.W), dbx, dbx ? bp : 0ull, pl);
 }
 
-// BF16 planes of the kept candidate (as prep32): split-packed words (word j
-// = symbol j | symbol j+32 << 16) -- DBX's from its row as they are, the
-// others built from the raw or compacted row.
+// BF16 planes of the kept candidate (as prep32, but ZBX's survivors are
+// compacted in place in the stage row): split-packed words (word j = symbol
+// j | symbol j+32 << 16) -- DBX's from its row as they are, the others built
+// from the raw or compacted row.
 __device__ __forceinline__ Prep prep16(uint32_t tag, uint32_t mlo, uint32_t mhi, uint32_t rowbase, uint32_t lane,
                                       uint32_t drow) {
   Prep pr{0u, 0u};
@@ -728,7 +738,10 @@ __device__ __forceinline__ Prep prep16(uint32_t tag, uint32_t mlo, uint32_t mhi,
   pr.base = lds16(stage_half(rowbase, lane, 0));
   pr.W = dbx ? 63u : 64u;
   if (tag == kTagZBX) {
-    uint32_t cnt = 0;  // compact the survivors' half-words in place (cnt <= h)
+    // the survivors' half-words compacted in place (cnt <= h); for 64
+    // half-words this loop over the survivors measured as fast as storing
+    // every half-word at its rank
+    uint32_t cnt = 0;
     for (uint32_t m = mlo; m; m &= m - 1, ++cnt)
       sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, __ffs(m) - 1)));
     for (uint32_t m = mhi; m; m &= m - 1, ++cnt)
