@@ -260,7 +260,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
 // Gray-coded deltas, split-packed the same way, go to the lane's DBX row.
 __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uint32_t cand, uint32_t drow) {
   uint32_t a = 0, b = 0, c = 0, adj = 0, andx = ~0u, ors = 0, gprev = 0, g0 = 0;
-  uint32_t mlo = 0, mhi = 0, zn = 0, adjz = 0, last = 0, fst = 0, seen = 0;
+  uint32_t mlo = 0, mhi = 0, zn = 0, adjz = 0, last = 0;
   uint32_t ad = 0, bd = 0, cd = 0, adjd = 0, andd = ~0u, ord = 0, Blo = 0, Bhi = 0, gdprev = 0,
            gd0 = 0, d32b = 0;
   const uint32_t s31lo = stage_unit(rowbase, lane, 3).w & 0xFFFF0000u;  // symbol 31 in the high half
@@ -282,8 +282,6 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     zn |= ~g & m;
     adjz |= last & g;
     last = (g & m) | (last & ~m);
-    fst |= g & ~seen;
-    seen |= m;
     // DBX: lo half d_j = s_j - s_{j-1}, hi half d_{j+32} = s_{j+32} - s_{j+31}
     uint32_t bo;
     const uint32_t d = sub16x2(x, xprev, bo);
@@ -315,8 +313,6 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     mhi = m >> 31;
     zn = ~g & m;
     last = g & m;
-    fst = g;
-    seen = m;
     uint32_t bo;
     uint32_t d = sub16x2(x, s31lo, bo);
     d &= 0xFFFF0000u;
@@ -378,7 +374,14 @@ __device__ __forceinline__ Sizes classify16(uint32_t rowbase, uint32_t lane, uin
     zbx = make_plan(0, 0, 0, 0, 0, 1, 0);
     z.s[kTagZBX] = 64;
   } else {
-    const uint32_t adjz16 = lo(adjz) | hi(adjz) | (lo(last) & hi(fst));
+    // the pair across the split: the last survivor among symbols 0..31 and
+    // the first among 32..63 (its Gray code read back from the stage row)
+    uint32_t gfirst = 0;
+    if (mhi) {
+      const uint32_t v = lds16(row_swz(rowbase, lane) ^ ((32u + (uint32_t)(__ffs(mhi) - 1)) << 1));
+      gfirst = v ^ (v >> 1);
+    }
+    const uint32_t adjz16 = lo(adjz) | hi(adjz) | (lo(last) & gfirst);
     const uint32_t A = ~(lo(zn) | hi(zn)) & a16;
     const int pn = (int)ceil_log2_u32((uint32_t)n);
     zbx = make_plan(a16, A, PX16, a16 & ~b16, b16 & ~c16 & adjz16, n, pn);
