@@ -12,8 +12,9 @@
 // shorten the transfer). Here the "engine" is the codec's kernels on the
 // caller's stream and the link is a copy stream: the tensor is cut into
 // pieces, and while piece k+1 is being compressed (decompressed), piece k is
-// on the link. Host code only; every byte is coded by the library's kernels
-// and moved by cudaMemcpyAsync.
+// on the link. Every byte is coded by the library's kernels and moved by
+// cudaMemcpyAsync; the only device code here is a one-thread kernel that
+// hands each piece's stream length to the host.
 //
 // Pieces: a first piece of half the largest piece P, then pieces of P, so
 // that the first piece's coding (swap-out) or transfer (swap-in), which
@@ -116,6 +117,25 @@ struct CopyDrain {
     if (armed) cudaStreamSynchronize(s);
   }
 };
+
+// A piece's stream length, from the encoder's total word into the
+// container's table in pinned host memory mapped for the device: stored by
+// the GPU, so that it does not queue on the copy engine behind the previous
+// piece's copy to the host (an 8-byte cudaMemcpyAsync would, and the host
+// needs the length before it can issue the piece's own copy).
+__global__ void store_length_kernel(const unsigned long long *src, unsigned long long *dst) { *dst = *src; }
+
+// The device address of host memory h if it is pinned and mapped, else null
+// (pageable memory gets its lengths by cudaMemcpyAsync).
+void *mapped_address(void *h) {
+  cudaPointerAttributes at;
+  void *d = nullptr;
+  if (cudaPointerGetAttributes(&at, h) != cudaSuccess || at.type != cudaMemoryTypeHost ||
+      cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess)
+    d = nullptr;
+  (void)cudaGetLastError();  // pageable memory is not an error of the call
+  return d;
+}
 
 // ------------------------------------------------------------ host layout
 
@@ -241,6 +261,7 @@ pz_status swap_out_core(HostSpan &span, const void *d_in, size_t nbytes, int ele
   for (size_t k = 0; k < n; ++k) table[2 * k] = sizes[k];
   *h_total = table_end(n);
   if (n == 0) return PZ_OK;
+  unsigned long long *table_dev = static_cast<unsigned long long *>(mapped_address(table));
 
   std::unique_lock<std::mutex> lk;
   Pipe *pipe = device_pipe(lk);
@@ -260,7 +281,16 @@ pz_status swap_out_core(HostSpan &span, const void *d_in, size_t nbytes, int ele
     if (k >= 2 && cudaStreamWaitEvent(s, pp.moved[b], 0) != cudaSuccess) return PZ_ERR_CUDA;
     const pz_status cs = pz_compress(in + at, sizes[k], elem_width, stage[b], sb, dlen + b, s);
     if (cs != PZ_OK) return cs;
-    if (cudaMemcpyAsync(table + 2 * k + 1, dlen + b, 8, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PZ_ERR_CUDA;
+    if (table_dev) {
+      const unsigned long long *src = dlen + b;
+      unsigned long long *dst = table_dev + 2 * k + 1;
+      void *args[2] = {&src, &dst};
+      if (cudaLaunchKernel(reinterpret_cast<const void *>(&store_length_kernel), dim3(1), dim3(1), args, 0, s) !=
+          cudaSuccess)
+        return PZ_ERR_CUDA;
+    } else if (cudaMemcpyAsync(table + 2 * k + 1, dlen + b, 8, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+      return PZ_ERR_CUDA;
+    }
     if (cudaEventRecord(pp.coded[b], s) != cudaSuccess) return PZ_ERR_CUDA;
     return PZ_OK;
   };
