@@ -178,11 +178,13 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width,
  * moved raw. Host memory should be pinned for the copies to overlap
  * (pageable memory works, serialised).
  *
- * Container (little-endian): a 32-byte head (u32 "PZS2", u32 pieces n, u64
+ * Container (little-endian): a 32-byte head (u32 "PZS3", u32 pieces n, u64
  * nbytes, u64 piece_bytes, u32 elem_width, u32 0), n entries of 16 bytes
  * (u64 raw bytes of the piece; u64 stored bytes, bit 63 set when the piece
  * is stored raw), then each piece -- its pz_compress stream, or its bytes --
- * at a 16-byte boundary.
+ * at a 128-byte boundary of the container (a copy to the device from a host
+ * address that is not 128-byte aligned is slower; give h_out, or the pool's
+ * memory, a 128-byte aligned start).
  *
  * Swap-out blocks the host until the container is complete (each piece's
  * stored length is needed on the host to copy it). Swap-in only enqueues:
@@ -197,7 +199,7 @@ size_t pz_swap_work_bytes(size_t piece_bytes);
 
 /* Host bytes pz_swap_out may write for nbytes in pieces of at most
  * piece_bytes (0 for an invalid piece size): the head and table plus every
- * piece's raw bytes rounded up to 16. Host-only, pure. */
+ * piece's raw bytes, each rounded up to 128. Host-only, pure. */
 size_t pz_swap_capacity(size_t nbytes, size_t piece_bytes);
 
 /* Swap out nbytes at d_in (device, 16-byte aligned) into the container at

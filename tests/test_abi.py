@@ -109,7 +109,8 @@ def test_swap_sizes_closed_forms(lib):
     for n, piece in ((0, 4096), (1, 4096), (4096, 4096), (4097, 4096), (10 << 20, 1 << 20), (3 << 20, 2 << 20),
                      (128 << 20, 32 << 20), (300_001, 65536), (10 << 20, 64 << 20)):
         sizes = piece_schedule(n, piece)
-        cap = (32 + 16 * len(sizes) + 15) // 16 * 16 + sum((r + 15) // 16 * 16 for r in sizes)
+        # the head and table, then every piece at a 128-byte boundary
+        cap = (32 + 16 * len(sizes) + 127) // 128 * 128 + sum((r + 127) // 128 * 128 for r in sizes)
         assert _lib.pz_swap_capacity(n, piece) == cap
 
 
@@ -129,14 +130,14 @@ def test_swap_argument_and_container_errors_are_host_side(lib):
     assert _lib.pz_swap_out(FAKE_IN, n, 4, piece, FAKE_OUT, work, h, cap - 1)[0] == _lib.PZ_ERR_CAPACITY
     # an empty tensor needs no device at all: the container is its head
     rc, total = _lib.pz_swap_out(0, 0, 4, piece, 0, 0, h, cap)
-    assert rc == _lib.PZ_OK and total == 32
-    assert struct.unpack_from("<IIQQII", host.raw, 0) == (0x32535A50, 0, 0, piece, 4, 0)
+    assert rc == _lib.PZ_OK and total == 128  # the head, rounded up to the pieces' 128-byte boundary
+    assert struct.unpack_from("<IIQQII", host.raw, 0) == (0x33535A50, 0, 0, piece, 4, 0)
     # swap-in rejects a container that does not match, before any device work:
     # a well-formed container of three 1 MiB pieces, each a 1 KB stream
-    head = struct.pack("<IIQQII", 0x32535A50, 3, n, piece, 4, 0) + struct.pack("<6Q", piece, 1024, piece, 1024,
+    head = struct.pack("<IIQQII", 0x33535A50, 3, n, piece, 4, 0) + struct.pack("<6Q", piece, 1024, piece, 1024,
                                                                                piece, 1024)
     ctypes.memmove(h, head, len(head))
-    ok_len = 80 + 3 * 1024
+    ok_len = 128 + 3 * 1024  # pieces from the table's end rounded up to 128
     assert _lib.pz_swap_in(h, ok_len, FAKE_OUT, work, FAKE_IN, n + 1, FAKE_WORD) == _lib.PZ_ERR_ARG   # nbytes
     assert _lib.pz_swap_in(h, 40, FAKE_OUT, work, FAKE_IN, n, FAKE_WORD) == _lib.PZ_ERR_ARG          # truncated
     bad = struct.pack("<IIQQII", 0x57535A50, 3, n, piece, 4, 0)
@@ -173,7 +174,7 @@ def test_pool_layout_and_host_side_errors(lib):
     assert _lib.pz_pool_swap_in(pool, 7, FAKE_OUT, 1 << 30, FAKE_IN, 4096, FAKE_WORD) == _lib.PZ_ERR_ARG
     # an empty tensor takes one slot (its head) and gives it back
     rc, t, stored = _lib.pz_pool_swap_out(pool, 0, 0, 4, 65536, 0, 0)
-    assert rc == _lib.PZ_OK and stored == 32 and _lib.pz_pool_free_slots(pool) == 4
+    assert rc == _lib.PZ_OK and stored == 128 and _lib.pz_pool_free_slots(pool) == 4
     assert _lib.pz_pool_release(pool, t) == _lib.PZ_OK and _lib.pz_pool_free_slots(pool) == 5
     assert _lib.pz_pool_release(pool, t) == _lib.PZ_ERR_ARG and _lib.pz_pool_free_slots(pool) == 5  # twice
     ts = [_lib.pz_pool_swap_out(pool, 0, 0, 2, 65536, 0, 0)[1] for _ in range(5)]

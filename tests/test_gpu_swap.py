@@ -33,15 +33,15 @@ def _built():
 
 def parse(container: bytes):
     magic, n, nbytes, piece, ew, zero = struct.unpack_from("<IIQQII", container, 0)
-    assert magic == 0x32535A50 and zero == 0
+    assert magic == 0x33535A50 and zero == 0
     entries = struct.unpack_from(f"<{2 * n}Q", container, 32)
-    off = (32 + 16 * n + 15) // 16 * 16
+    off = (32 + 16 * n + 127) // 128 * 128  # pieces at 128-byte boundaries
     pieces = []
     for k in range(n):
         raw, stored = entries[2 * k], entries[2 * k + 1]
         L = stored & ~RAW_FLAG
         pieces.append((raw, bool(stored & RAW_FLAG), container[off: off + L]))
-        off += (L + 15) // 16 * 16
+        off += (L + 127) // 128 * 128
     return nbytes, piece, ew, pieces, off
 
 
@@ -130,7 +130,7 @@ def test_swap_in_reports_a_malformed_piece():
     _, _, _, pieces, _ = parse(bufs.host[:length].numpy().tobytes())
     n = len(pieces)
     assert n == 3 and not pieces[1][1]
-    off = (32 + 16 * n + 15) // 16 * 16 + (len(pieces[0][2]) + 15) // 16 * 16  # piece 1's stream
+    off = (32 + 16 * n + 127) // 128 * 128 + (len(pieces[0][2]) + 127) // 128 * 128  # piece 1's stream
     bufs.host[off: off + 2] = 0  # chunk 0 of piece 1 claims L = 0
     out = torch.empty_like(x)
     st = bufs.swap_in(length, out)
