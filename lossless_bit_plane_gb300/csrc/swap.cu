@@ -88,8 +88,10 @@ size_t stage_bytes(size_t piece) { return align16(pz_max_compressed_bytes(piece)
 // kept; a mutex per device serialises swap calls on that device.
 struct Pipe {
   cudaStream_t copy = nullptr;
-  cudaEvent_t coded[2] = {nullptr, nullptr};  // caller's stream: piece coded / decoded out of stage b
+  cudaStream_t dec2 = nullptr;  // swap-in: the decodes out of stage 1 (stage 0's run on the caller's stream)
+  cudaEvent_t coded[2] = {nullptr, nullptr};  // piece coded / decoded out of stage b
   cudaEvent_t moved[2] = {nullptr, nullptr};  // copy stream: stage b (or the raw piece) moved
+  cudaEvent_t joined = nullptr;               // swap-in: the second decode stream's end
   bool ok = false;
 };
 constexpr int kMaxDevices = 64;
@@ -103,7 +105,9 @@ Pipe *device_pipe(std::unique_lock<std::mutex> &lk) {
   lk = std::unique_lock<std::mutex>(g_pipe_mu[dev]);
   Pipe &p = g_pipe[dev];
   if (!p.ok) {
-    bool ok = cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking) == cudaSuccess;
+    bool ok = cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.dec2, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.joined, cudaEventDisableTiming) == cudaSuccess;
     for (int i = 0; i < 2 && ok; ++i)
       ok = cudaEventCreateWithFlags(&p.coded[i], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&p.moved[i], cudaEventDisableTiming) == cudaSuccess;
@@ -393,9 +397,12 @@ pz_status swap_in_core(const HostSpan &span, size_t h_bytes, void *d_work, size_
   const size_t sb = stage_bytes(P);
   uint8_t *stage[2] = {work, work + sb};
   uint8_t *out = static_cast<uint8_t *>(d_out);
-  // the link may start as soon as the caller's earlier work is done
-  if (cudaEventRecord(pp.coded[0], s) != cudaSuccess || cudaStreamWaitEvent(pp.copy, pp.coded[0], 0) != cudaSuccess)
+  // the link and the second decode stream may start as soon as the
+  // caller's earlier work is done
+  if (cudaEventRecord(pp.coded[0], s) != cudaSuccess || cudaStreamWaitEvent(pp.copy, pp.coded[0], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(pp.dec2, pp.coded[0], 0) != cudaSuccess)
     return PZ_ERR_CUDA;
+  CopyDrain drain2{pp.dec2};
   std::vector<size_t> at(n + 1), dst(n + 1);
   at[0] = table_end(n);
   dst[0] = 0;
@@ -404,9 +411,11 @@ pz_status swap_in_core(const HostSpan &span, size_t h_bytes, void *d_work, size_
     dst[k + 1] = dst[k] + raw[k];
   }
   // The coded pieces alternate between the two stages (the j-th coded piece
-  // in stage j%2). A coded piece is moved into its stage once the coded piece
-  // two before it has been decoded out of that stage; a raw piece is moved
-  // straight to its place in d_out and waits for nothing.
+  // in stage j%2), and the decodes out of stage 1 run on a second stream, so
+  // that one piece's walk may overlap the previous piece's decode. A coded
+  // piece is moved into its stage once the coded piece two before it has
+  // been decoded out of that stage; a raw piece is moved straight to its
+  // place in d_out and waits for nothing.
   std::vector<int> sidx(n, -1);
   for (size_t k = 0, j = 0; k < n; ++k)
     if (!(stored[k] & kRawFlag)) sidx[k] = (int)(j++);
@@ -437,15 +446,20 @@ pz_status swap_in_core(const HostSpan &span, size_t h_bytes, void *d_work, size_
     if (k + 1 < n && (st = move(k + 1)) != PZ_OK) return st;  // the next piece moves while this one decodes
     if (stored[k] & kRawFlag) continue;
     const int b = sidx[k] & 1;
-    if (cudaStreamWaitEvent(s, pp.moved[b], 0) != cudaSuccess) return PZ_ERR_CUDA;
-    st = pz::decompress_launch(stage[b], stored[k], elem_width, out + dst[k], raw[k], d_status, s, false);
+    const cudaStream_t ds = b ? pp.dec2 : s;
+    if (cudaStreamWaitEvent(ds, pp.moved[b], 0) != cudaSuccess) return PZ_ERR_CUDA;
+    st = pz::decompress_launch(stage[b], stored[k], elem_width, out + dst[k], raw[k], d_status, ds, false);
     if (st != PZ_OK) return st;
-    if (cudaEventRecord(pp.coded[b], s) != cudaSuccess) return PZ_ERR_CUDA;
+    if (cudaEventRecord(pp.coded[b], ds) != cudaSuccess) return PZ_ERR_CUDA;
   }
+  // the caller's stream waits for the second decode stream
+  if (cudaEventRecord(pp.joined, pp.dec2) != cudaSuccess || cudaStreamWaitEvent(s, pp.joined, 0) != cudaSuccess)
+    return PZ_ERR_CUDA;
   // the caller's stream waits for the last copies (the raw pieces' too)
   if (cudaEventRecord(pp.moved[0], pp.copy) != cudaSuccess || cudaStreamWaitEvent(s, pp.moved[0], 0) != cudaSuccess)
     return PZ_ERR_CUDA;
   drain.armed = false;
+  drain2.armed = false;
   return PZ_OK;
 }
 
