@@ -312,8 +312,10 @@ class SwapPool:
         if self.work_bytes == 0:
             raise ValueError("piece_bytes must be a positive multiple of 4096")
         self.work = torch.empty(self.work_bytes, dtype=torch.uint8, device=device)
-        self.host = torch.empty(pool_bytes + 64, dtype=torch.uint8).pin_memory()
-        base = (self.host.data_ptr() + 63) // 64 * 64
+        # a 4096-byte aligned base: the slots (and so the container's pieces,
+        # at 128-byte boundaries of the container) start aligned
+        self.host = torch.empty(pool_bytes + 4096, dtype=torch.uint8).pin_memory()
+        base = (self.host.data_ptr() + 4095) // 4096 * 4096
         rc, self.pool = pz_pool_init(base, pool_bytes, slot_bytes)
         if rc != PZ_OK:
             raise PlaneZipError("pz_pool_init", rc)
