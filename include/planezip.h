@@ -243,9 +243,9 @@ size_t pz_pool_bytes(size_t slot_bytes, size_t nslots);
  * slots as fit). The slots lie at 4096-byte offsets from h_mem: with h_mem
  * 4096-byte aligned (pinned allocations are), every piece of a pooled
  * container starts 128-byte aligned in host memory, which copies to the
- * device need for the link's full rate. *pool points into h_mem; the pool needs no teardown
- * beyond freeing h_mem once no call uses it. Errors: PZ_ERR_ARG,
- * PZ_ERR_CAPACITY (not one slot fits). */
+ * device need for the link's full rate. *pool points into h_mem; the pool
+ * needs no teardown beyond freeing h_mem once no call uses it. Errors:
+ * PZ_ERR_ARG, PZ_ERR_CAPACITY (not one slot fits). */
 pz_status pz_pool_init(void *h_mem, size_t bytes, size_t slot_bytes,
                        pz_pool **pool);
 
