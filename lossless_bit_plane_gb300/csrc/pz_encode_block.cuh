@@ -34,32 +34,6 @@ __device__ __forceinline__ int run_cost(uint64_t Z, int K) {
   return 3 * S + (2 + K) * (R - S);
 }
 
-// Cost of the non-zero planes NZ of width W (position field p): planes that
-// are all ones or whose pre-XOR plane is zero (c5) take the 5-bit code, or
-// verbatim if shorter; planes with one or two adjacent ones take 5 + p (or
-// verbatim); the rest are verbatim, 1 + W.
-__device__ __forceinline__ int nonzero_cost(uint64_t NZ, uint64_t A, uint64_t PX, uint64_t ST,
-                                            int W, int p) {
-  uint64_t c5 = (A | PX) & NZ;
-  uint64_t cm = ST & NZ & ~c5;
-  uint64_t cv = NZ & ~(c5 | cm);
-  int lv = 1 + W;
-  int l5 = min(5, lv), lm = min(5 + p, lv);
-  return l5 * __popcll(c5) + lm * __popcll(cm) + lv * __popcll(cv);
-}
-
-// Class of a single plane given as a word: 0 zero, else its code length.
-template <typename T>
-__device__ __forceinline__ int single_plane_len(T X, T full, int W, int p) {
-  if (X == 0) return 0;
-  int ones = (sizeof(T) == 8) ? __popcll((uint64_t)X) : __popc((uint32_t)X);
-  int lv = 1 + W;
-  if (X == full) return min(5, lv);
-  bool adj2 = (ones == 2) && ((X & (X >> 1)) != 0);
-  if (ones == 1 || adj2) return min(5 + p, lv);
-  return lv;
-}
-
 // Class of every plane of one candidate (bit i = plane i): non-zero, and the
 // code each non-zero plane takes: verbatim, a 5-bit code (all-ones or, if
 // not all-ones, pre-XOR-zero), or a 5+p-bit position code (single one or,
@@ -132,26 +106,6 @@ __device__ __forceinline__ uint32_t row_swz(uint32_t rowbase, uint32_t r) { retu
 __device__ __forceinline__ uint4 stage_unit(uint32_t rowbase, uint32_t r, uint32_t u) {  // u < 8
   return lds128(row_swz(rowbase, r) ^ (u << 4));
 }
-__device__ __forceinline__ uint32_t unit_word(const uint4 &q, int k) {
-  return (k == 0) ? q.x : (k == 1) ? q.y : (k == 2) ? q.z : q.w;
-}
-// The block's 32 words into registers (FP32), or its split-packed words
-// (BF16: word j = symbol j | symbol j+32 << 16).
-template <bool W16>
-__device__ __forceinline__ void load_block(uint32_t rowbase, uint32_t lane, uint32_t (&s)[32]) {
-  uint32_t raw[32];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint4 q = stage_unit(rowbase, lane, u);
-    raw[4 * u] = q.x;
-    raw[4 * u + 1] = q.y;
-    raw[4 * u + 2] = q.z;
-    raw[4 * u + 3] = q.w;
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) s[j] = W16 ? split_word(raw, j) : raw[j];
-}
-
 // The lane's row of DBX words: 32 words in a 128-byte-aligned row, 16-byte
 // units swizzled like a stage row (unit u at u ^ (lane & 7)). The classifier
 // leaves there, as it streams the block, the Gray-coded deltas that DBX codes
@@ -162,8 +116,8 @@ __device__ __forceinline__ uint32_t drow_unit(uint32_t drow, uint32_t lane, uint
 }
 
 // ------------------------------------------------------------ FP32 classify
-// s: the block's 32 symbols. Returns the five candidate sizes (tag excluded).
-// The words are streamed from the stage row four at a time, so that only the
+// The five candidate sizes (tag excluded) of the lane's block of 32 symbols
+// and the kept candidate's plan. The words are streamed from the stage row four at a time, so that only the
 // accumulators stay in registers; DBX's Gray-coded deltas go to the lane's
 // DBX row (drow) unit by unit.
 __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uint32_t cand, uint32_t drow) {
@@ -254,7 +208,7 @@ __device__ __forceinline__ Sizes classify32(uint32_t rowbase, uint32_t lane, uin
 }
 
 // ------------------------------------------------------------ BF16 classify
-// sp: split-packed block (word j = symbol j | symbol j+32 << 16).
+// As classify32 for a block of 64 BF16 symbols, on split-packed words.
 // Split-packed words (word j = symbol j | symbol j+32 << 16) are built while
 // streaming the stage row: word j needs raw words j/2 and 16 + j/2. DBX's
 // Gray-coded deltas, split-packed the same way, go to the lane's DBX row.
