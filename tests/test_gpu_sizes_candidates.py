@@ -42,6 +42,24 @@ MASKS = {
 }
 
 
+def survivors_every_count(ew: int, seed: int) -> np.ndarray:
+    """Blocks with n non-zero symbols of random value for every n from 0 to
+    the block's symbol count, twice each: restricted to ZBX (or DBX, BX) the
+    verbatim plane codes then come in every plane width, and whole groups of
+    four verbatim planes in every width (the encoder writes those in one
+    step: as pairs of codes up to 31 bits, as five or nine words at 32 and
+    64 bits, as four codes of up to 64 bits for BF16 ZBX)."""
+    rng = np.random.default_rng(seed)
+    nsym, dt = (32, np.uint32) if ew == 4 else (64, np.uint16)
+    blocks = []
+    for n in range(nsym + 1):
+        for _ in range(2):
+            b = np.zeros(nsym, dtype=dt)
+            b[rng.choice(nsym, n, replace=False)] = rng.integers(1, 1 << (8 * ew), n, dtype=np.uint64).astype(dt)
+            blocks.append(b)
+    return np.concatenate(blocks)
+
+
 def _data():
     rng = np.random.default_rng(21)
     relu = W.relu_values(3 * 32768 + 1000, rng)                            # ~388 KB FP32, ragged tail
@@ -55,6 +73,8 @@ def _data():
         ("conv_bf16", conv, 2),
         ("attention_bf16", att, 2),
         ("tiny_bf16", W.tiny_alphabet_blocks(256, "bf16"), 2),
+        ("survivors_fp32", survivors_every_count(4, 31), 4),
+        ("survivors_bf16", survivors_every_count(2, 32), 2),
     ]
 
 
