@@ -182,9 +182,9 @@ pz_status pz_compressed_size(const void *d_in, size_t nbytes, int elem_width,
  * nbytes, u64 piece_bytes, u32 elem_width, u32 0), n entries of 16 bytes
  * (u64 raw bytes of the piece; u64 stored bytes, bit 63 set when the piece
  * is stored raw), then each piece -- its pz_compress stream, or its bytes --
- * at a 128-byte boundary of the container (a copy to the device from a host
- * address that is not 128-byte aligned is slower; give h_out, or the pool's
- * memory, a 128-byte aligned start).
+ * at a 128-byte boundary of the container, the bytes between pieces zero (a
+ * copy to the device from a host address that is not 128-byte aligned is
+ * slower; give h_out, or the pool's memory, a 128-byte aligned start).
  *
  * Swap-out blocks the host until the container is complete (each piece's
  * stored length is needed on the host to copy it). Swap-in only enqueues:

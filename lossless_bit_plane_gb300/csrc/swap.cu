@@ -160,6 +160,18 @@ struct HostSpan {
   uint8_t *at(size_t x, size_t &run) const;
   // Make container bytes [0, end) addressable (pool: take slots).
   pz_status reserve(size_t end);
+  // Zero container bytes [x, x + len) on the host (the padding after a
+  // piece, so that a container's bytes depend on the tensor alone).
+  void zero(size_t x, size_t len) const {
+    while (len) {
+      size_t run = 0;
+      uint8_t *h = at(x, run);
+      const size_t m = std::min(run, len);
+      std::memset(h, 0, m);
+      x += m;
+      len -= m;
+    }
+  }
   // One copy per contiguous run between container bytes [x, x + len) and a
   // device buffer.
   pz_status copy(size_t x, void *dev, size_t len, cudaMemcpyKind kind, cudaStream_t s) const {
@@ -322,6 +334,11 @@ pz_status swap_out_core(HostSpan &span, const void *d_in, size_t nbytes, int ele
                         pp.copy)) != PZ_OK)
       return st;
     if (!raw && cudaEventRecord(pp.moved[b], pp.copy) != cudaSuccess) return PZ_ERR_CUDA;
+    const size_t pad = align_piece(stored) - stored;  // outside the bytes the copy writes
+    if (pad) {
+      if ((st = span.reserve(off + stored + pad)) != PZ_OK) return st;
+      span.zero(off + stored, pad);
+    }
     off += align_piece(stored);
     src += sizes[k];
   }

@@ -93,6 +93,35 @@ def test_swap_round_trip_and_pieces_equal_the_oracle(name, make, ew, piece):
     check_pieces(raw, ew, piece, pieces)
 
 
+def test_swap_through_pageable_host_memory():
+    # a pageable container: the pieces' lengths reach the host by copies
+    # instead of the kernel stores used for pinned memory; same container,
+    # same round trip
+    arr = W.relu_values(200_000, np.random.default_rng(23))
+    raw = arr.view(np.uint8)
+    x = torch.from_numpy(raw.copy()).cuda()
+    piece = 256 * 1024
+    work_bytes = _lib.pz_swap_work_bytes(piece)
+    work = torch.empty(work_bytes, dtype=torch.uint8, device="cuda")
+    cap = _lib.pz_swap_capacity(raw.size, piece)
+    host = np.zeros(cap + 128, dtype=np.uint8)  # pageable
+    h = (host.ctypes.data + 127) // 128 * 128
+    rc, length = _lib.pz_swap_out(x.data_ptr(), raw.size, 4, piece, work.data_ptr(), work_bytes, h, cap)
+    assert rc == _lib.PZ_OK
+    off = h - host.ctypes.data
+    container = host[off: off + length].tobytes()
+    _, _, _, pieces, end = parse(container)
+    assert end == length
+    check_pieces(raw, 4, piece, pieces)
+    _, pinned_container = roundtrip(arr, 4, piece)
+    assert container == pinned_container
+    out = torch.empty_like(x)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert _lib.pz_swap_in(h, length, work.data_ptr(), work_bytes, out.data_ptr(), raw.size, st.data_ptr()) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(out, x)
+
+
 def test_incompressible_tensor_is_moved_raw():
     rng = np.random.default_rng(7)
     raw, container = roundtrip(rng.integers(0, 256, 3 << 20, dtype=np.uint8), 4, 1 << 20)
