@@ -50,7 +50,7 @@ WORKLOAD = ("1 GiB throughput sweep: {ReLU, smooth conv, causal attention} x {FP
 NCU_ENCODER_TRAFFIC = {
     "sources": ("lossless_bit_plane_gb300/csrc/encode.cu", "lossless_bit_plane_gb300/csrc/pz_encode_block.cuh",
                 "lossless_bit_plane_gb300/csrc/pz_device.cuh", "lossless_bit_plane_gb300/csrc/pz_format.cuh"),
-    "sources_sha256": "8a4286fff4d2d608c8b456c2fab997470145d420e94eec1258ddeb8dc0879607",
+    "sources_sha256": "7cb094d412af3a3f3b45de534fcc91266be76b006f19d1cbb717d98764a4b20f",
     "bytes_per_launch": 212.01e6,
 }
 

@@ -27,10 +27,12 @@
 //    flags are plain OR/AND accumulations across words. BF16 runs the same
 //    word loop on two 16-bit symbols per word (symbols j and j+32).
 //  - Only the winning candidate is materialised: its planes come from one
-//    32x32 bit transpose in registers, and its codes go into a shared chunk
-//    buffer through an LSB-first writer at the block's bit offset (a warp
-//    prefix sum over the lanes' block sizes), plane by plane with every lane
-//    of the warp at the same plane.
+//    32x32 bit transpose in registers (DBX's deltas as the classifier left
+//    them in the lane's row of the output region), and its codes go into a
+//    shared chunk buffer through an LSB-first writer at the block's bit
+//    offset (a warp prefix sum over the lanes' block sizes), four planes at a
+//    time with every lane of the warp at the same four planes: four
+//    verbatim planes in one step, the others one by one.
 //  - Chunk offsets come from a single-pass decoupled look-back over 8-byte
 //    status words (flag | value) in the scratch tail of the output buffer,
 //    with a bounded spin; the warp then copies its chunk to its final byte
