@@ -518,8 +518,10 @@ __device__ __forceinline__ bool coop_walk(const uint32_t *stage, uint32_t bit0, 
     while (i >= 0) {
       // lane k holds the 64 bits at the k-th code ahead, were the codes
       // before it verbatim; its lowest bit is that code's flag
-      const uint32_t q = bit0 + pos + lane * S, qi = q >> 5;
-      const uint32_t x0 = word(qi), x1 = word(qi + 1), x2 = word(qi + 2);
+      // one clamp for the three words (a malformed stream cannot read past
+      // the stage; a valid one never reaches the clamp)
+      const uint32_t q = bit0 + pos + lane * S, qi = min(q >> 5, kCoopStageWords - 3u);
+      const uint32_t x0 = stage[qi], x1 = stage[qi + 1], x2 = stage[qi + 2];
       const uint32_t lo = __funnelshift_r(x0, x1, q & 31u), hi = __funnelshift_r(x1, x2, q & 31u);
       const uint32_t f = __ballot_sync(0xFFFFFFFFu, lo & 1u);
       const int m = (f == 0xFFFFFFFFu) ? 32 : __ffs(~f) - 1;  // leading verbatim codes
