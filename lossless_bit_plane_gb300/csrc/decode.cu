@@ -260,10 +260,11 @@ __device__ __forceinline__ bool walk_warp(const DecodeArgs &p, bool walk, uint64
   constexpr uint32_t w = W16 ? 16u : 32u;   // bits per symbol = BX planes
   constexpr uint32_t N = W16 ? 64u : 32u;   // symbols per block
   constexpr uint32_t K = W16 ? 4u : 5u;     // run field
-  // flags tested per plane step: 14 (FP32) and 10 (BF16) measured fastest on
-  // the sweep's activations; fewer flags mean more iterations, more flags
-  // more loads per iteration than the verbatim runs repay
-  constexpr uint32_t kSkip = W16 ? 10u : 14u;
+  // flags tested per plane step. FP32: 26, so that a block's trailing run of
+  // verbatim planes (the mantissa's, after its last short codes) takes one
+  // step; with 14 to 25 flags it takes two, and more than 26 add loads that
+  // no run repays. BF16: 10 (12 was no faster), fewer mean more iterations.
+  constexpr uint32_t kSkip = W16 ? 10u : 26u;
   // bits an iteration may read past its position: five words at the
   // position, or a plane block's header fields (tag and mask, or tag and
   // base), two codes of at most 11 bits each and kSkip flags N + 1 apart
