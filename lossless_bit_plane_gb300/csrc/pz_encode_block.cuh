@@ -611,7 +611,8 @@ __device__ __forceinline__ void emit_plane_codes(PosWriter &wr, uint32_t rowbase
 // buffer (the DBX rows lie in it): the candidate's words -- DBX's
 // Gray-coded deltas from the lane's DBX row, the block's words (BX) from the
 // stage row, or its survivors (ZBX), stored in order at their ranks into the
-// lane's DBX row, which ZBX does not need, Gray-coded here --
+// lane's DBX row, which ZBX does not need (read from the stage row instead
+// where they are the block's first W symbols already), Gray-coded here --
 // go through one 32x32 bit transpose into the stage row as plane rows
 // (store_planes). Every lane runs the same loads, from a row picked by its
 // candidate. Returns the plane width W (0: no plane codes) and, for DBX,
@@ -627,7 +628,10 @@ __device__ __forceinline__ Prep prep32(uint32_t tag, uint32_t nz, uint32_t rowba
   const bool dbx = (tag == kTagDBX);
   pr.base = lds32(stage_word(rowbase, lane, 0));
   pr.W = dbx ? 31u : 32u;
-  if (tag == kTagZBX) {  // the survivors, in order, to the lane's DBX row (which ZBX does not use)
+  // survivors that are the block's first W symbols (a causal mask's rows)
+  // are in place already: the planes come from the stage row as for BX
+  const bool moved = (tag == kTagZBX) && (nz & (nz + 1u)) != 0u;
+  if (moved) {  // the survivors, in order, to the lane's DBX row (which ZBX does not use)
     const uint32_t dx = row_swz(drow, lane);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -639,10 +643,10 @@ __device__ __forceinline__ Prep prep32(uint32_t tag, uint32_t nz, uint32_t rowba
         if (nz & (1u << j)) sts32(dx ^ ((uint32_t)__popc(nz & ((1u << j) - 1u)) << 2), w[k]);
       }
     }
-    pr.W = (uint32_t)__popc(nz);
   }
+  if (tag == kTagZBX) pr.W = (uint32_t)__popc(nz);
   // DBX rows are Gray-coded already (row bit j = delta j, bit 0 zero)
-  const uint32_t src = (tag == kTagBX) ? rowbase : drow, gmask = dbx ? 0u : 0xFFFFFFFFu;
+  const uint32_t src = (dbx || moved) ? drow : rowbase, gmask = dbx ? 0u : 0xFFFFFFFFu;
   uint32_t T[32];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
@@ -697,13 +701,17 @@ __device__ __forceinline__ Prep prep16(uint32_t tag, uint32_t mlo, uint32_t mhi,
   if (tag == kTagZBX) {
     // the survivors' half-words compacted in place (cnt <= h); for 64
     // half-words this loop over the survivors measured as fast as storing
-    // every half-word at its rank
-    uint32_t cnt = 0;
-    for (uint32_t m = mlo; m; m &= m - 1, ++cnt)
-      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, __ffs(m) - 1)));
-    for (uint32_t m = mhi; m; m &= m - 1, ++cnt)
-      sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, 31 + __ffs(m))));
-    pr.W = cnt;
+    // every half-word at its rank. Survivors that are the block's first W
+    // symbols (a causal mask's rows) are in place already.
+    const bool prefix = (mhi == 0u) ? (mlo & (mlo + 1u)) == 0u : (mlo == ~0u && (mhi & (mhi + 1u)) == 0u);
+    if (!prefix) {
+      uint32_t cnt = 0;
+      for (uint32_t m = mlo; m; m &= m - 1, ++cnt)
+        sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, __ffs(m) - 1)));
+      for (uint32_t m = mhi; m; m &= m - 1, ++cnt)
+        sts16(stage_half(rowbase, lane, cnt), lds16(stage_half(rowbase, lane, 31 + __ffs(m))));
+    }
+    pr.W = (uint32_t)(__popc(mlo) + __popc(mhi));
   }
   const uint32_t src = dbx ? drow : rowbase, gmask = dbx ? 0u : 0x7FFF7FFFu;
   uint32_t R[32], T[32];
