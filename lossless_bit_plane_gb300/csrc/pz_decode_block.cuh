@@ -212,7 +212,9 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
         o[j] = prev;
         prev += d;
       }
-    } else if (tag == kTagZBX) {
+    } else if (tag == kTagZBX && (mlo & (mlo + 1u)) != 0u) {
+      // (survivors that are the block's first W symbols -- a causal mask's
+      // rows -- are in place already, and the planes' bits from W on are 0)
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (j < W) sts32(prow(row, lane, j), o[j]);
@@ -240,7 +242,9 @@ __device__ __forceinline__ bool decode_block(const StageBits &sb, uint32_t &q, u
       o[j] = (o[j] & 0xFFFFu) | (prev << 16);
       prev = (prev + d) & 0xFFFFu;
     }
-  } else if (tag == kTagZBX) {
+  } else if (tag == kTagZBX && !((mhi == 0u) ? (mlo & (mlo + 1u)) == 0u : (mlo == ~0u && (mhi & (mhi + 1u)) == 0u))) {
+    // (survivors that are the block's first W symbols are in place already,
+    // zeros after them: the split words become raw words below, as for BX)
     // survivors t_0..t_{W-1}: t_j in o[j] low, t_{j+32} in o[j] high. They
     // go to the lane's row as half-words in index order (word m = t_2m |
     // t_2m+1 << 16, the same pairing as a raw word), and each raw word of
