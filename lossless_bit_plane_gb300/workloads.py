@@ -359,4 +359,20 @@ def tiny_alphabet_blocks(nblocks: int, dtype: str, seed: int = 7) -> np.ndarray:
     return TINY_ALPHABET_32[rng.integers(0, 6, nblocks * 32)].astype("<u4").view(np.uint8)
 
 
+
+def verbatim_run_blocks(nchunks: int, elem_width: int, seed: int = 89) -> np.ndarray:
+    """Blocks whose symbols share their top k bits (a constant of the block)
+    over uniform random low bits, k cycling through 0..w across blocks (w =
+    8 x elem_width): the top k planes are constant and the low w - k random,
+    so coded blocks carry verbatim-plane runs of every length."""
+    rng = _rng(seed)
+    w = 8 * elem_width
+    nblk = nchunks * 32
+    k = (np.arange(nblk, dtype=np.uint64) % np.uint64(w + 1))[:, None]
+    lowmask = (np.uint64(1) << (np.uint64(w) - k)) - np.uint64(1)
+    low = rng.integers(0, 1 << w, (nblk, 128 // elem_width), dtype=np.uint64)
+    top = rng.integers(0, 1 << w, (nblk, 1), dtype=np.uint64)
+    vals = (top & ~lowmask) | (low & lowmask)
+    return vals.astype("<u4" if elem_width == 4 else "<u2").view(np.uint8).reshape(-1)
+
 TAIL_SIZES = (0, 2, 4, 126, 128, 130, 4094, 4096, 4098)

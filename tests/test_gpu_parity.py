@@ -142,30 +142,16 @@ def test_config4_mlp_ln_full(dtype):
         _large_case(t)
 
 
-def _verbatim_run_blocks(nchunks, ew, seed):
-    # Every 128-byte block: its symbols share their top k bits (a constant of
-    # the block) over random low bits, k cycling through 0..w across blocks.
-    # The top k planes are then constant (short codes) and the low w - k
-    # planes random (verbatim codes), so a walk meets verbatim runs of every
-    # length: shorter than, equal to and longer than the flags one step tests.
-    rng = np.random.default_rng(seed)
-    w = 8 * ew
-    nblk = nchunks * 32
-    k = (np.arange(nblk, dtype=np.uint64) % np.uint64(w + 1))[:, None]
-    lowmask = (np.uint64(1) << (np.uint64(w) - k)) - np.uint64(1)
-    low = rng.integers(0, 1 << w, (nblk, 128 // ew), dtype=np.uint64)
-    top = rng.integers(0, 1 << w, (nblk, 1), dtype=np.uint64)
-    vals = (top & ~lowmask) | (low & lowmask)
-    return vals.astype(np.uint32 if ew == 4 else np.uint16).view(np.uint8).reshape(-1)
-
-
 @pytest.mark.parametrize("ew", [4, 2])
 @pytest.mark.parametrize("nchunks", [1000, 5000, 6300])
 def test_verbatim_runs_of_every_length_on_each_walk(nchunks, ew):
     # 1,000 chunks: the fused walk and decode; 5,000: the cooperative walk;
     # 6,300: the thread walk. Whole stream against the oracle, then the
     # round trip.
-    data = _verbatim_run_blocks(nchunks, ew, seed=89 + nchunks + ew)
+    # Blocks whose top k planes are constant and whose low planes are random,
+    # k cycling through 0..w: verbatim runs of every length, shorter than,
+    # equal to and longer than the flags one walk step tests.
+    data = W.verbatim_run_blocks(nchunks, ew, seed=89 + nchunks + ew)
     t = W.Tensor(f"verbatim_runs_{nchunks}_{ew}", "fp32" if ew == 4 else "bf16", data)
     _large_case(t)
     lens = np.frombuffer(oracle_parallel.compress(data, ew)[: 2 * nchunks], dtype=np.uint16)

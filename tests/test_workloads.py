@@ -138,3 +138,25 @@ def test_same_seed_same_bytes():
     c = W.attention_bf16(batch=1, heads=1, seq=32)
     d = W.attention_bf16(batch=1, heads=1, seq=32)
     assert np.array_equal(c.data, d.data)
+
+
+def test_verbatim_run_blocks_give_runs_of_every_length():
+    # The recipe's premise, checked with the oracle's per-block analysis:
+    # blocks sharing k top bits over random low bits take BX (or DBX) with
+    # w - k verbatim planes, so the coded blocks span run lengths on both
+    # sides of the walks' flag windows (26 for 32-bit, 10 for 16-bit symbols).
+    import oracle
+
+    for ew, bx_ks in ((4, range(2, 11)), (2, range(1, 16))):
+        w = 8 * ew
+        data = W.verbatim_run_blocks(4, ew, seed=5)
+        assert data.size == 4 * 4096
+        tags = np.asarray(oracle.analyze(data, ew)[0]).reshape(-1)
+        for b, t in enumerate(tags):
+            if b % (w + 1) in bx_ks:
+                assert int(t) == oracle.TAG_BX, (ew, b)
+        sym = data.view("<u4" if ew == 4 else "<u2").reshape(-1, 128 // ew).astype(np.uint64)
+        for b in range(tags.size):
+            k = b % (w + 1)
+            if k:  # the top k bits are the block's own constant
+                assert np.unique(sym[b] >> np.uint64(w - k)).size == 1
